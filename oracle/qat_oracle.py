@@ -1,0 +1,315 @@
+"""Plain, slow fp64 CPU oracle for quantization-aware attention (QAT attention).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference arm of ``bench.py`` may import this module.  The product
+path (the CUDA library and its Python binding) never imports, calls or links it,
+and this module imports nothing from the product package.
+
+What it computes, per (batch b, head h, query row i), over the valid keys
+V_i = {j < Nkv, and j <= i when causal}:
+
+  s_ij   = sm_scale * <q_i, k_j>
+  m_i    = max_j s_ij,  e_ij = exp(s_ij - m_i),  l_i = sum_j e_ij,  P_ij = e_ij / l_i
+  O_hp,i = sum_j P_ij v_j                       (the straight-through output)
+  lse_i  = (m_i + ln l_i) / ln 2                (base-2 log-sum-exp)
+  quant tile t of row i = {j in V_i : floor(j / 64) = t}, T_it = max_{j in t} s_ij
+  c_ij   = E4M3_RNE_SATFINITE(448 * exp(s_ij - T_it))
+  Pq_ij  = c_ij * exp(T_it - m_i) / 448 / l_i
+  O_q,i  = sum_j Pq_ij v_j                      (the returned output)
+
+Sources (page titles and sections):
+  * "attn_qat_train.py" (FastVideo fastvideo-kernel), ``_attn_fwd_inner``: online
+    base-2 softmax with qk_scale = sm_scale * log2(e), exp2 of the shifted scores,
+    ``fake_quantize`` of P per (query rows x KV tile), the row sum l taken from the
+    *unquantized* P, and two accumulators (quantized and high precision).
+  * same page, ``_attn_fwd`` epilogue: ``m_i += log2(l_i)`` stored as M (base 2), and
+    both accumulators divided by l_i.
+  * same page, ``_attn_bwd_preprocess``: Delta_i = sum_d O_id dO_id.
+  * same page, ``_attn_bwd_dkdv`` / ``_attn_bwd_dq``: P rematerialized from the saved
+    statistic, dP = dO V^T, dS = P o (dP - Delta), dK = sm_scale dS^T Q,
+    dQ = sm_scale dS K, dV = P^T dO.
+  * "support for pytorch autograd" (SageAttention issue 60): the backward is built by
+    rematerialization, as for FlashAttention.
+
+Readings where the pages are silent (``quant_utils`` is imported but not shown):
+  * FP8 format: OCP E4M3 (bias 7, max 448, subnormal step 2^-9), round to nearest
+    even, saturating to +-448.
+  * Scale: absmax / 448 per (query row x 64-key tile); tiles aligned to absolute key 0.
+  * Masked / padded keys are excluded from the tile max, from l and from O.
+  * Straight-through estimator: the backward differentiates L = <dO, O_hp>, i.e.
+    quantization is treated as the identity; Delta uses O_hp; dV uses unquantized P.
+
+The fp32 quantization primitive (``quant_tiles_fp32``) is the bit-level rule the
+CUDA kernels follow for one row x 64-key tile of fp32 probabilities:
+  amax = max p; if amax == 0: scale 0, codes 0, values 0;
+  else inv = fl32(448 / amax), scale = fl32(amax / 448) (IEEE round-to-nearest),
+  code = E4M3_RNE_SATFINITE(fl32(p * inv)), value = bf16_rn(fl32(decode(code) * scale)).
+In exact arithmetic code depends only on p / amax, so it equals the definition above.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, brute force, library routines, finite differences) except
+fidelity to the pages' own ``fake_quantize`` — parity unpinned, because its source
+(``quant_utils``) is not on the pages.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+E4M3_MAX = 448.0          # largest finite OCP E4M3 value: 2^8 * 1.75
+E4M3_MIN_NORMAL_EXP = -6  # exponent of the smallest normal E4M3 value (2^-6)
+E4M3_MANT_BITS = 3
+QUANT_TILE = 64           # keys per quantization tile (absolute key alignment)
+LN2 = math.log(2.0)
+
+
+# ---------------------------------------------------------------------------
+# OCP FP8 E4M3
+# ---------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each E4M3 byte (OCP OFP8): sign bit 7, exponent bits 6..3 (bias 7),
+    mantissa bits 2..0; exponent 0 is subnormal (2^-6 * m / 8); 0x7F / 0xFF are NaN."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    sub = np.ldexp(m / 8.0, np.full_like(e, E4M3_MIN_NORMAL_EXP))
+    val = sign * np.where(e == 0, sub, normal)
+    return np.where((c & 0x7F) == 0x7F, np.nan, val)
+
+
+def e4m3_rne_satfinite(x) -> tuple[np.ndarray, np.ndarray]:
+    """Round finite reals to E4M3 with round-to-nearest-even, saturating to +-448.
+
+    Returns (code bytes as uint8, value as float64).  The rounding quantum of a value
+    with binary exponent e is 2^(max(e, -6) - 3); dividing by a power of two and
+    ``np.rint`` (ties to even) are exact, so the result is the correctly rounded one.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, E4M3_MIN_NORMAL_EXP)
+    quantum = np.ldexp(1.0, e - E4M3_MANT_BITS)
+    q = np.rint(a / quantum) * quantum
+    q = np.minimum(q, E4M3_MAX)
+    # encode q (exactly representable by construction)
+    _, qex = np.frexp(q)
+    qe = qex - 1
+    is_norm = q >= 2.0 ** E4M3_MIN_NORMAL_EXP
+    mant_norm = np.rint(np.ldexp(q, -qe) * 8.0 - 8.0)
+    code_norm = ((qe + 7) << 3) + mant_norm.astype(np.int64)
+    code_sub = np.rint(q / 2.0 ** -9).astype(np.int64)
+    code = np.where(is_norm, code_norm, code_sub)
+    code = np.where(np.signbit(x) & (q > 0), code | 0x80, code)
+    return code.astype(np.uint8), np.copysign(q, x)
+
+
+# ---------------------------------------------------------------------------
+# bf16 helpers (the oracle's own; nothing shared with the product)
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) exactly to float64."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def f32_to_bf16_rn(x) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns float32 values."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# The fp32 quantization primitive for row x 64-key tiles
+# ---------------------------------------------------------------------------
+
+def quant_tiles_fp32(p) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Fake-quantize fp32 tiles row by row: p has shape [rows, cols] (one tile per row).
+
+    Returns (deq float32 [rows, cols] = bf16-rounded quantized values,
+             scale float32 [rows] = amax / 448,
+             codes uint8 [rows, cols]).
+    All arithmetic is IEEE float32 with round-to-nearest, as the rule states.
+    """
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    amax = p.max(axis=1)
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
+    inv = (np.float32(E4M3_MAX) / safe).astype(np.float32)
+    scale = (safe / np.float32(E4M3_MAX)).astype(np.float32)
+    x = (p * inv[:, None]).astype(np.float32)
+    codes, vals = e4m3_rne_satfinite(x.astype(np.float64))
+    deq32 = (vals.astype(np.float32) * scale[:, None]).astype(np.float32)
+    deq = f32_to_bf16_rn(deq32)
+    codes = np.where(nz[:, None], codes, np.uint8(0)).astype(np.uint8)
+    deq = np.where(nz[:, None], deq, np.float32(0)).astype(np.float32)
+    scale = np.where(nz, scale, np.float32(0)).astype(np.float32)
+    return deq, scale, codes
+
+
+# ---------------------------------------------------------------------------
+# Forward (fp64) for one (b, h) head
+# ---------------------------------------------------------------------------
+
+def _valid_mask(rows: np.ndarray, nkv: int, causal: bool) -> np.ndarray:
+    cols = np.arange(nkv)
+    if causal:
+        return cols[None, :] <= rows[:, None]
+    return np.ones((rows.size, nkv), dtype=bool)
+
+
+def head_forward(q, k, v, sm_scale: float, causal: bool, quant: bool,
+                 rows=None, return_p: bool = False):
+    """fp64 forward of one head.
+
+    q [Nq, D], k/v [Nkv, D] (float64).  ``rows`` selects query rows (default all);
+    rows are independent, so a subset is the same definition applied to fewer i.
+    Returns dict with o_hp, o_q (if quant), lse (base 2), and optionally p / pq.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    nq, nkv = q.shape[0], k.shape[0]
+    rows = np.arange(nq) if rows is None else np.asarray(rows)
+    valid = _valid_mask(rows, nkv, causal)
+    s = sm_scale * (q[rows] @ k.T)                              # s_ij
+    s_m = np.where(valid, s, -np.inf)
+    m = s_m.max(axis=1)                                         # m_i
+    e = np.where(valid, np.exp(s_m - m[:, None]), 0.0)          # e_ij
+    l = e.sum(axis=1)                                           # l_i (unquantized)
+    p = e / l[:, None]                                          # P_ij
+    out = {"o_hp": p @ v, "lse": (m + np.log(l)) / LN2, "m": m, "l": l}
+    if return_p:
+        out["p"] = p
+    if quant:
+        pq = np.zeros_like(p)
+        ntiles = (nkv + QUANT_TILE - 1) // QUANT_TILE
+        for t in range(ntiles):
+            lo, hi = t * QUANT_TILE, min(nkv, (t + 1) * QUANT_TILE)
+            st = s_m[:, lo:hi]
+            vt = valid[:, lo:hi]
+            has = vt.any(axis=1)
+            T = np.where(has, st.max(axis=1), 0.0)              # T_it
+            ratio = np.where(vt, np.exp(st - T[:, None]), 0.0)  # exp(s_ij - T_it)
+            _, c = e4m3_rne_satfinite(E4M3_MAX * ratio)         # c_ij (values)
+            w = np.where(has, np.exp(T - m) / E4M3_MAX / l, 0.0)
+            pq[:, lo:hi] = c * w[:, None]                       # Pq_ij
+        out["o_q"] = pq @ v
+        if return_p:
+            out["pq"] = pq
+    return out
+
+
+def forward(q, k, v, sm_scale: float, causal: bool, quant: bool, row_chunk: int = 2048):
+    """fp64 forward over [B, H, N, D] arrays; returns (o_q, o_hp, lse) (o_q None if not quant)."""
+    B, H, nq, D = q.shape
+    o_hp = np.zeros((B, H, nq, D))
+    o_q = np.zeros((B, H, nq, D)) if quant else None
+    lse = np.zeros((B, H, nq))
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, nq, row_chunk):
+                rows = np.arange(r0, min(nq, r0 + row_chunk))
+                r = head_forward(q[b, h], k[b, h], v[b, h], sm_scale, causal, quant, rows)
+                o_hp[b, h, rows] = r["o_hp"]
+                lse[b, h, rows] = r["lse"]
+                if quant:
+                    o_q[b, h, rows] = r["o_q"]
+    return o_q, o_hp, lse
+
+
+# ---------------------------------------------------------------------------
+# Backward (fp64, straight-through estimator) for one (b, h) head
+# ---------------------------------------------------------------------------
+
+def head_backward(q, k, v, do, sm_scale: float, causal: bool):
+    """Gradients of L = <dO, O_hp> with respect to q, k, v for one head (fp64).
+
+    Delta_i = sum_d dO_id O_hp,id ; dP = dO V^T ; dS = P o (dP - Delta) ;
+    dQ = sm_scale dS K ; dK = sm_scale dS^T Q ; dV = P^T dO.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    f = head_forward(q, k, v, sm_scale, causal, quant=False, return_p=True)
+    p, o_hp = f["p"], f["o_hp"]
+    delta = (do * o_hp).sum(axis=1)
+    dp = do @ v.T
+    ds = p * (dp - delta[:, None])
+    return sm_scale * (ds @ k), sm_scale * (ds.T @ q), p.T @ do
+
+
+def backward(q, k, v, do, sm_scale: float, causal: bool):
+    """fp64 STE backward over [B, H, N, D] arrays; returns (dq, dk, dv)."""
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            dq[b, h], dk[b, h], dv[b, h] = head_backward(
+                q[b, h], k[b, h], v[b, h], do[b, h], sm_scale, causal)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Sampled checks for long sequences (same definitions, fewer outputs)
+# ---------------------------------------------------------------------------
+
+def head_row_stats(q, k, sm_scale: float, causal: bool, row_chunk: int = 1024):
+    """m_i and l_i for every query row of one head, rows taken in independent chunks."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    nq, nkv = q.shape[0], k.shape[0]
+    m = np.empty(nq)
+    l = np.empty(nq)
+    for r0 in range(0, nq, row_chunk):
+        rows = np.arange(r0, min(nq, r0 + row_chunk))
+        valid = _valid_mask(rows, nkv, causal)
+        s = np.where(valid, sm_scale * (q[rows] @ k.T), -np.inf)
+        m[rows] = s.max(axis=1)
+        l[rows] = np.exp(s - m[rows][:, None]).sum(axis=1)
+    return m, l
+
+
+def head_backward_sampled(q, k, v, do, sm_scale: float, causal: bool,
+                          q_rows, kv_rows, row_chunk: int = 1024):
+    """dQ at rows ``q_rows`` and dK / dV at key rows ``kv_rows`` of one head (fp64).
+
+    Uses the same formulas as ``head_backward``; O_hp and Delta are needed for every
+    query row because dK_j and dV_j sum over all i, so they are formed chunk by chunk.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    nq, nkv = q.shape[0], k.shape[0]
+    q_rows = np.asarray(q_rows)
+    kv_rows = np.asarray(kv_rows)
+    m, l = head_row_stats(q, k, sm_scale, causal, row_chunk)
+    delta = np.empty(nq)
+    p_cols = np.empty((nq, kv_rows.size))      # P[:, kv_rows]
+    for r0 in range(0, nq, row_chunk):
+        rows = np.arange(r0, min(nq, r0 + row_chunk))
+        valid = _valid_mask(rows, nkv, causal)
+        s = np.where(valid, sm_scale * (q[rows] @ k.T), -np.inf)
+        p = np.exp(s - m[rows][:, None]) / l[rows][:, None]
+        delta[rows] = (do[rows] * (p @ v)).sum(axis=1)
+        p_cols[rows] = p[:, kv_rows]
+    dp_cols = do @ v[kv_rows].T                                 # dP[:, kv_rows]
+    ds_cols = p_cols * (dp_cols - delta[:, None])
+    dk = sm_scale * (ds_cols.T @ q)
+    dv = p_cols.T @ do
+    valid = _valid_mask(q_rows, nkv, causal)
+    s = np.where(valid, sm_scale * (q[q_rows] @ k.T), -np.inf)
+    p = np.exp(s - m[q_rows][:, None]) / l[q_rows][:, None]
+    ds = p * (do[q_rows] @ v.T - delta[q_rows][:, None])
+    dq = sm_scale * (ds @ k)
+    return dq, dk, dv

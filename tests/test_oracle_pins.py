@@ -1,0 +1,303 @@
+"""Pins for the fp64 oracle, checked against facts outside the oracle itself:
+the OCP E4M3 table, brute-force nearest-value search, closed forms, invariants,
+torch's own float64 SDPA / autograd (library routines) and finite differences.
+CPU only."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import qat_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers (test side)
+
+def _all_finite_codes():
+    """Every non-negative finite E4M3 code and its value, decoded here bit by bit."""
+    codes, vals = [], []
+    for c in range(0x7F):                     # 0x7F is NaN
+        e, m = (c >> 3) & 0xF, c & 7
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        codes.append(c)
+        vals.append(v)
+    return np.array(codes), np.array(vals)
+
+
+def nearest_e4m3(x):
+    """Brute force: the finite E4M3 value nearest to x >= 0, ties to the even code,
+    values above the largest finite value saturate."""
+    codes, vals = _all_finite_codes()
+    if x >= vals.max():
+        return int(codes[np.argmax(vals)]), float(vals.max())
+    d = np.abs(vals - x)
+    best = np.flatnonzero(d == d.min())
+    if best.size > 1:
+        best = [b for b in best if codes[b] % 2 == 0]
+    b = best[0]
+    return int(codes[b]), float(vals[b])
+
+
+def rng_f64(seed, *shape, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(np.ravel(a - b)) / np.linalg.norm(np.ravel(b)))
+
+
+# ---------------------------------------------------------------- E4M3
+
+def test_e4m3_golden_table():
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "e4m3_ocp_values.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    codes = np.array([int(c, 16) for c, _ in rows])
+    want = np.array([float(v) for _, v in rows])
+    got = orc.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    assert np.array_equal(got[fin], want[fin])
+    # encoding the finite values gives back their codes
+    c2, v2 = orc.e4m3_rne_satfinite(want[fin])
+    assert np.array_equal(c2, codes[fin].astype(np.uint8))
+    assert np.array_equal(v2, want[fin])
+
+
+def test_e4m3_rne_matches_bruteforce_nearest():
+    codes, vals = _all_finite_codes()
+    vals_sorted = np.sort(vals)
+    mids = (vals_sorted[1:] + vals_sorted[:-1]) / 2          # exact ties
+    rnd = np.abs(np.random.default_rng(7).standard_normal(3000)) * 40
+    tiny = np.abs(np.random.default_rng(8).standard_normal(500)) * 2 ** -8
+    big = np.array([448.0, 455.9, 464.0, 470.0, 479.9, 480.0, 1e6])
+    xs = np.concatenate([vals, mids, np.nextafter(mids, 0), np.nextafter(mids, 1e9),
+                         rnd, tiny, big, [0.0, 2.0 ** -10, 2.0 ** -10 * 1.0001]])
+    got_c, got_v = orc.e4m3_rne_satfinite(xs)
+    for x, c, v in zip(xs, got_c, got_v):
+        wc, wv = nearest_e4m3(float(x))
+        assert (int(c), float(v)) == (wc, wv), x
+    # decode/encode round trip over every finite code, both signs
+    allc = np.concatenate([codes, codes[1:] | 0x80])
+    dec = orc.e4m3_decode(allc)
+    c3, v3 = orc.e4m3_rne_satfinite(dec)
+    assert np.array_equal(c3, allc.astype(np.uint8)) and np.array_equal(v3, dec)
+
+
+# ---------------------------------------------------------------- fp32 quant primitive
+
+def _bf16_rn_scalar(x32):
+    u = int(np.float32(x32).view(np.uint32))
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return float(np.uint32(u).view(np.float32))
+
+
+def test_quant_primitive_matches_scalar_loop():
+    rng = np.random.default_rng(3)
+    p = np.exp(rng.standard_normal((40, 64)) * 3).astype(np.float32)
+    p[5] = 0.0                                   # empty tile
+    p[6, :10] = 0.0
+    p[7] = np.float32(1e-30) * p[7]              # tiny but normal amax
+    deq, scale, codes = orc.quant_tiles_fp32(p)
+    for r in range(p.shape[0]):
+        amax = np.float32(max(p[r]))
+        if amax == 0:
+            assert scale[r] == 0 and not codes[r].any() and not deq[r].any()
+            continue
+        inv = np.float32(448.0) / amax
+        s = amax / np.float32(448.0)
+        assert scale[r] == s
+        for c in range(64):
+            x = np.float32(p[r, c] * inv)
+            wc, wv = nearest_e4m3(float(x))
+            assert codes[r, c] == wc
+            assert deq[r, c] == _bf16_rn_scalar(np.float32(np.float32(wv) * s))
+
+
+def test_quant_primitive_max_maps_to_448_and_scale_invariance():
+    rng = np.random.default_rng(4)
+    p = np.exp(rng.standard_normal((32, 64)) * 2).astype(np.float32)
+    deq, scale, codes = orc.quant_tiles_fp32(p)
+    am = p.argmax(axis=1)
+    assert np.all(codes[np.arange(32), am] == 0x7E)
+    for k in (-20, -3, 1, 7):
+        d2, s2, c2 = orc.quant_tiles_fp32(p * np.float32(2.0 ** k))
+        assert np.array_equal(c2, codes)
+        assert np.array_equal(s2, scale * np.float32(2.0 ** k))
+        assert np.array_equal(d2, deq * np.float32(2.0 ** k))
+
+
+def test_quant_primitive_idempotent_codes():
+    rng = np.random.default_rng(5)
+    p = np.exp(rng.standard_normal((64, 64)) * 2).astype(np.float32)
+    deq, _, codes = orc.quant_tiles_fp32(p)
+    _, _, codes2 = orc.quant_tiles_fp32(deq)
+    assert np.array_equal(codes, codes2)
+
+
+# ---------------------------------------------------------------- forward
+
+def _sdpa64(q, k, v, scale, causal):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    return torch.nn.functional.scaled_dot_product_attention(
+        t(q), t(k), t(v), scale=scale, is_causal=causal).numpy()
+
+
+@pytest.mark.parametrize("nq,nkv,d,causal", [(37, 37, 16, False), (37, 37, 16, True),
+                                              (20, 150, 8, False), (130, 9, 32, False)])
+def test_forward_hp_equals_library_sdpa_and_lse(nq, nkv, d, causal):
+    q, k, v = rng_f64(1, 2, 3, nq, d), rng_f64(2, 2, 3, nkv, d), rng_f64(3, 2, 3, nkv, d)
+    sc = 1 / math.sqrt(d)
+    _, o_hp, lse = orc.forward(q, k, v, sc, causal, quant=False, row_chunk=16)
+    assert np.allclose(o_hp, _sdpa64(q, k, v, sc, causal), rtol=1e-12, atol=1e-12)
+    s = torch.from_numpy(q) @ torch.from_numpy(k).transpose(-1, -2) * sc
+    if causal:
+        s = s.masked_fill(torch.ones(nq, nkv, dtype=torch.bool).triu(1), -math.inf)
+    want = (torch.logsumexp(s, dim=-1) / math.log(2)).numpy()
+    assert np.allclose(lse, want, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_rows_of_p_sum_to_one_and_causal_zeros():
+    q, k, v = rng_f64(4, 50, 8), rng_f64(5, 50, 8), rng_f64(6, 50, 8)
+    r = orc.head_forward(q, k, v, 0.4, True, quant=True, return_p=True)
+    assert np.allclose(r["p"].sum(axis=1), 1.0, atol=1e-13)
+    upper = np.triu(np.ones((50, 50), dtype=bool), 1)
+    assert not r["p"][upper].any() and not r["pq"][upper].any()
+
+
+def test_forward_identical_keys_closed_form():
+    nkv, d = 200, 16
+    q, v = rng_f64(7, 9, d), rng_f64(8, nkv, d)
+    k = np.tile(rng_f64(9, 1, d), (nkv, 1))
+    sc = 0.3
+    r = orc.head_forward(q, k, v, sc, False, quant=True)
+    assert np.allclose(r["o_hp"], v.mean(axis=0)[None], rtol=0, atol=1e-13)
+    assert np.allclose(r["o_q"], v.mean(axis=0)[None], rtol=0, atol=1e-13)
+    want_lse = sc * (q @ k[0]) / math.log(2) + math.log2(nkv)
+    assert np.allclose(r["lse"], want_lse, rtol=0, atol=1e-12)
+
+
+def test_forward_causal_ignores_future_keys():
+    n, d = 70, 8
+    q, k, v = rng_f64(10, n, d), rng_f64(11, n, d), rng_f64(12, n, d)
+    a = orc.head_forward(q, k, v, 0.5, True, quant=True)
+    k2, v2 = k.copy(), v.copy()
+    k2[40:] += 5.0
+    v2[40:] -= 3.0
+    b = orc.head_forward(q, k2, v2, 0.5, True, quant=True)
+    for key in ("o_q", "o_hp", "lse"):
+        assert np.array_equal(a[key][:40], b[key][:40])
+        assert not np.allclose(a[key][41:], b[key][41:])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_quantized_output_bruteforce(causal):
+    """O_q from a pure-Python loop: per row, per absolute 64-key tile, code by
+    brute-force nearest search, weight exp(T - m) / 448 / l."""
+    n, d = 150, 4                              # 3 tiles, ragged tail of 22 keys
+    q, k, v = rng_f64(13, n, d, scale=2.0), rng_f64(14, n, d), rng_f64(15, n, d)
+    sc = 0.7
+    r = orc.head_forward(q, k, v, sc, causal, quant=True)
+    want = np.zeros((n, d))
+    for i in range(n):
+        keys = [j for j in range(n) if (j <= i or not causal)]
+        s = {j: sc * float(q[i] @ k[j]) for j in keys}
+        m = max(s.values())
+        l = sum(math.exp(s[j] - m) for j in keys)
+        for t in range(3):
+            tk = [j for j in keys if j // 64 == t]
+            if not tk:
+                continue
+            T = max(s[j] for j in tk)
+            for j in tk:
+                _, c = nearest_e4m3(448.0 * math.exp(s[j] - T))
+                want[i] += c * math.exp(T - m) / 448.0 / l * v[j]
+    assert np.allclose(r["o_q"], want, rtol=1e-12, atol=1e-12)
+    assert rel_l2(r["o_q"], r["o_hp"]) < 0.05
+
+
+def _quant_p_exact(p, tile=64):
+    """The quantization of an already-normalized P row block, step by step (fp64)."""
+    out = np.zeros_like(p)
+    for lo in range(0, p.shape[1], tile):
+        blk = p[:, lo:lo + tile]
+        amax = blk.max(axis=1, keepdims=True)
+        _, c = orc.e4m3_rne_satfinite(448.0 * blk / np.where(amax > 0, amax, 1))
+        out[:, lo:lo + tile] = c * amax / 448.0
+    return out
+
+
+def test_forward_quant_idempotent_and_matches_p_form():
+    n, d = 130, 8
+    q, k, v = rng_f64(16, n, d, scale=1.5), rng_f64(17, n, d), rng_f64(18, n, d)
+    r = orc.head_forward(q, k, v, 0.6, False, quant=True, return_p=True)
+    pq = _quant_p_exact(r["p"])
+    assert np.allclose(r["pq"], pq, rtol=1e-12, atol=0)
+    assert np.allclose(_quant_p_exact(pq), pq, rtol=1e-13, atol=0)
+
+
+def test_forward_row_chunking_is_transparent():
+    q, k, v = rng_f64(19, 1, 2, 77, 8), rng_f64(20, 1, 2, 77, 8), rng_f64(21, 1, 2, 77, 8)
+    a = orc.forward(q, k, v, 0.3, True, quant=True, row_chunk=5)
+    b = orc.forward(q, k, v, 0.3, True, quant=True, row_chunk=1000)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- backward (STE)
+
+@pytest.mark.parametrize("nq,nkv,causal", [(23, 23, False), (23, 23, True), (9, 70, False)])
+def test_backward_matches_torch_autograd_fp64(nq, nkv, causal):
+    d = 16
+    q, k, v = rng_f64(22, 2, 2, nq, d), rng_f64(23, 2, 2, nkv, d), rng_f64(24, 2, 2, nkv, d)
+    do = rng_f64(25, 2, 2, nq, d)
+    sc = 1 / math.sqrt(d)
+    tq, tk, tv = (torch.from_numpy(a).requires_grad_(True) for a in (q, k, v))
+    s = tq @ tk.transpose(-1, -2) * sc
+    if causal:
+        s = s.masked_fill(torch.ones(nq, nkv, dtype=torch.bool).triu(1), -math.inf)
+    o = torch.softmax(s, dim=-1) @ tv
+    o.backward(torch.from_numpy(do))
+    dq, dk, dv = orc.backward(q, k, v, do, sc, causal)
+    for got, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        assert np.allclose(got, ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_finite_differences(causal):
+    n, d = 6, 5
+    q, k, v, do = (rng_f64(30 + i, n, d) for i in range(4))
+    sc = 0.45
+    dq, dk, dv = orc.head_backward(q, k, v, do, sc, causal)
+
+    def loss(qq, kk, vv):
+        return float((do * orc.head_forward(qq, kk, vv, sc, causal, quant=False)["o_hp"]).sum())
+
+    h = 1e-6
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert np.allclose(grad, num, rtol=1e-6, atol=1e-8)
+
+
+def test_backward_sampled_equals_full():
+    n, d = 90, 8
+    q, k, v, do = (rng_f64(40 + i, n, d) for i in range(4))
+    for causal in (False, True):
+        dq, dk, dv = orc.head_backward(q, k, v, do, 0.35, causal)
+        rows, keys = np.array([0, 7, 63, 64, 89]), np.array([1, 30, 88])
+        sq, sk, sv = orc.head_backward_sampled(q, k, v, do, 0.35, causal, rows, keys, row_chunk=17)
+        assert np.allclose(sq, dq[rows], rtol=1e-12, atol=1e-13)
+        assert np.allclose(sk, dk[keys], rtol=1e-12, atol=1e-13)
+        assert np.allclose(sv, dv[keys], rtol=1e-12, atol=1e-13)
+        m, l = orc.head_row_stats(q, k, 0.35, causal, row_chunk=13)
+        f = orc.head_forward(q, k, v, 0.35, causal, quant=False)
+        assert np.allclose(f["m"], m) and np.allclose(f["l"], l)
