@@ -1,0 +1,386 @@
+"""Benchmark of the QAT attention hot path (forward + straight-through backward).
+
+One step = qat_attn_fwd + qat_attn_bwd over the video-DiT workload
+B=1, H=40, Nq=Nkv=32768, D=128, non-causal, P fake-quantized to FP8 E4M3 per
+query row x 64-key tile, on seeded synthetic N(0, 1) bf16 inputs resident in HBM.
+Each input tensor (335 MB) is larger than L2 (129 MB), so no L2 flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Metric: TFLOP/s counting the algorithmic flops of the
+method, 16 * pairs * D per step (forward 3 GEMMs = 6 pairs D: QK^T, quant(P) V, P V;
+backward 5 GEMMs = 10 pairs D: QK^T, dO V^T, P^T dO, dS^T Q, dS K).
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload (the host-core reference arm).  Under torchrun each rank runs its own copy of
+the workload (weak scaling; no data-path collective).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "QAT attention fwd+bwd TFLOPS (% of GB300 bf16 tensor peak) at seq 32K, d=128"
+UNIT = "TFLOP/s"
+WORKLOAD = "c4"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w):
+    return {
+        "workload": (f"{w.name}: video-DiT self-attention B={w.B} H={w.H} Nq=Nkv={w.Nq} "
+                     f"D={w.D} non-causal, P fake-quant FP8 E4M3 per row x 64-key tile"),
+        "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D, "causal": w.causal,
+        "sm_scale": "1/sqrt(D)", "quant_mode": "fp8e4m3_row_tile64",
+        "l2": "inputs larger than L2 (335 MB per tensor vs 129 MB L2); no flush",
+        "flops_per_step": "16*pairs*D (fwd 6, bwd 10)",
+    }
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_sample_tflops(w, rows: int, seed: int = 0):
+    """Times the fp64 oracle on one head of the workload: ``rows`` query rows against all
+    keys, forward (with quantization) and backward.  Returns (tflops, seconds, pairs)."""
+    import numpy as np
+
+    from oracle import qat_oracle as orc
+    rng = np.random.default_rng(1000 * w.idx + 7 + seed)
+
+    def bf16(shape):
+        x = rng.standard_normal(size=shape, dtype=np.float32)
+        u = x.view(np.uint32).astype(np.uint64)
+        return orc.bf16_bits_to_f64(((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16))
+
+    q, do = bf16((rows, w.D)), bf16((rows, w.D))
+    k, v = bf16((w.Nkv, w.D)), bf16((w.Nkv, w.D))
+    t0 = time.perf_counter()
+    orc.head_forward(q, k, v, w.sm_scale, False, quant=True)
+    orc.head_backward(q, k, v, do, w.sm_scale, False)
+    dt = time.perf_counter() - t0
+    pairs = rows * w.Nkv
+    return 16.0 * pairs * w.D / dt / 1e12, dt, pairs
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    rows = 256
+    for _ in range(args.warmup):
+        oracle_sample_tflops(w, rows)
+    vals, secs = [], 0.0
+    for s in range(args.steps):
+        tf, dt, _ = oracle_sample_tflops(w, rows, seed=s)
+        vals.append(tf)
+        secs += dt
+    value = statistics.median(vals)
+    sample = (f"one head of {w.name}: {rows} query rows x {w.Nkv} keys, D={w.D}, fp64 forward "
+              f"(with FP8 quantization) + backward per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs widened to fp64)",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import torch.distributed as tdist
+
+    from quantization_aware_attention_gb300 import build as qbuild
+    from quantization_aware_attention_gb300 import capi
+    from quantization_aware_attention_gb300.inputs import make_inputs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU; the library has no CPU path")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        tdist.init_process_group("nccl", device_id=dev)
+    qbuild.build() if rank == 0 else None
+    if world > 1:
+        tdist.barrier()
+    capi.lib()
+
+    B, H, Nq, Nkv, D = w.B, w.H, w.Nq, w.Nkv, w.D
+    inp = make_inputs(w)
+    host = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+            for n, a in inp.items()}
+    del inp
+    x = {n: t.to(dev) for n, t in host.items()}
+    o_q = torch.empty_like(x["q"])
+    o_hp = torch.empty_like(x["q"])
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(x["q"])
+    dk = torch.empty_like(x["k"])
+    dv = torch.empty_like(x["v"])
+    ws_bytes = capi.qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sm = w.sm_scale
+    launches_per_step = 4  # fwd kernel; bwd preprocess, dK/dV kernel, dQ kernel
+
+    def fwd():
+        st = capi.qat_attn_fwd(x["q"], x["k"], x["v"], o_q, o_hp, lse, B, H, Nq, Nkv, D, sm,
+                               0, capi.QUANT_P_FP8E4M3_ROW_TILE64, stream)
+        if st != capi.Status.OK:
+            raise capi.QatError(st, "qat_attn_fwd")
+
+    def bwd():
+        st = capi.qat_attn_bwd(x["q"], x["k"], x["v"], o_hp, lse, x["do"], dq, dk, dv, B, H, Nq,
+                               Nkv, D, sm, 0, capi.QUANT_P_FP8E4M3_ROW_TILE64, ws, ws_bytes,
+                               stream)
+        if st != capi.Status.OK:
+            raise capi.QatError(st, "qat_attn_bwd")
+
+    def barrier():
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident timing
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    clocks = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        fwd()
+        e1.record(stream)
+        bwd()
+        e2.record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    fwd_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in ev)
+    bwd_ms = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in ev)
+    if capi.qat_attn_device_status(stream) != capi.Status.OK:
+        raise RuntimeError("a kernel reported an expired bounded wait")
+
+    pairs = w.pairs
+    flops_step = 16.0 * pairs * D
+    ms_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: host buffers, copies inside the timed region
+    hout = {n: torch.empty(host["q"].shape, dtype=torch.bfloat16).pin_memory()
+            for n in ("o_q", "dq")}
+    hout.update({n: torch.empty(host["k"].shape, dtype=torch.bfloat16).pin_memory()
+                 for n in ("dk", "dv")})
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_step():
+        for n, t in host.items():
+            x[n].copy_(t, non_blocking=True)
+        fwd()
+        bwd()
+        hout["o_q"].copy_(o_q, non_blocking=True)
+        hout["dq"].copy_(dq, non_blocking=True)
+        hout["dk"].copy_(dk, non_blocking=True)
+        hout["dv"].copy_(dv, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(s0.elapsed_time(s1))
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel work (the backward call)
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bwd_tf = 10.0 * pairs * D / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = 6.0 * pairs * D / (fwd_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, see quantization_aware_attention_gb300/inputs.py)",
+        "config": workload_config(w),
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_frac_of_burst_peak": fwd_tf / peak_burst,
+        "bwd_frac_of_burst_peak": bwd_tf / peak_burst,
+        "tflops_flash_convention": world * 14.0 * pairs * D * args.steps / (total_ms * 1e-3) / 1e12,
+        "tokens_per_s": world * B * Nq * args.steps / (total_ms * 1e-3),
+        "roofline": {
+            "kernel": "qat_attn_bwd call (preprocess + dK/dV + dQ kernels)",
+            "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
+            "frac": bwd_tf / peak_sus, "traffic": None,
+            "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+            "algorithmic_flops_per_launch": 10.0 * pairs * D,
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = 2048
+        tf, dt, _ = oracle_sample_tflops(w, rows)
+        line["cpu_baseline"] = {
+            "value": tf, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"one head of {w.name}: {rows} query rows x {w.Nkv} keys, fp64 forward "
+                       f"(with FP8 quantization) + backward, {dt:.1f} s; numpy BLAS matmuls, "
+                       f"elementwise steps single-threaded")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        tdist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    from quantization_aware_attention_gb300.inputs import WORKLOADS
+    w = WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

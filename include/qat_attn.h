@@ -1,0 +1,155 @@
+/*
+ * qat_attn.h -- C ABI of the GB300 (sm_103a) quantization-aware attention library.
+ *
+ * The library computes training-time scaled-dot-product attention whose softmax
+ * probabilities P are fake-quantized to FP8 E4M3 with an absmax scale per
+ * (query row x 64-key tile), keeping a straight-through high-precision output beside
+ * the quantized one, and the matching backward.
+ *
+ * Sources (page titles and sections):
+ *   "attn_qat_train.py" (FastVideo fastvideo-kernel):
+ *     _attn_fwd_inner   online base-2 softmax, fake_quantize(P), l from unquantized P,
+ *                       two accumulators (quantized and high precision);
+ *     _attn_fwd         epilogue: M = m + log2(l) (base 2), both outputs divided by l;
+ *     _attn_bwd_preprocess  Delta = rowsum(O * dO);
+ *     _attn_bwd_dkdv, _attn_bwd_dq, _attn_bwd  dV, dP, dS, dK, dQ with P rematerialized;
+ *     _attention.forward / .backward  the host contract (save q, k, v, O, M).
+ *   "support for pytorch autograd" (SageAttention issue 60): backward by
+ *     rematerialization, as for FlashAttention.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, contiguous, row-major; bf16 tensors are [B, H, N, D] with D
+ *     innermost.  "bf16" buffers hold IEEE bfloat16 bit patterns.
+ *   - All pointers are DEVICE pointers unless stated otherwise, 16-byte aligned.
+ *   - The caller owns every buffer.  The library allocates no device memory on these
+ *     paths and keeps no per-call state; it caches only its loaded kernels and the
+ *     SM count of each device.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  A QAT_OK return means the work was enqueued.
+ *   - Nothing throws across the ABI; every failure is a status code.  Arguments are
+ *     validated on the host before anything is enqueued.
+ */
+#ifndef QAT_ATTN_H
+#define QAT_ATTN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define QAT_API __attribute__((visibility("default")))
+#else
+#define QAT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QAT_OK = 0,
+  QAT_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, bad D or mode   */
+  QAT_ERR_UNSUPPORTED = 2, /* valid request this library does not implement       */
+  QAT_ERR_CUDA = 3,        /* a CUDA runtime / launch error (see cudaGetLastError) */
+  QAT_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (kernel returned)  */
+  QAT_ERR_WORKSPACE = 5    /* workspace missing or smaller than required            */
+} qat_status_t;
+
+/* quant_mode values */
+enum {
+  QAT_QUANT_NONE = 0,                /* O_q is computed with P unquantized (= O_hp) */
+  QAT_QUANT_P_FP8E4M3_ROW_TILE64 = 1 /* P fake-quantized per row x 64-key tile      */
+};
+
+/*
+ * qat_attn_fwd -- forward pass.
+ *   ("attn_qat_train.py", _attn_fwd and _attn_fwd_inner.)
+ *
+ *   q      bf16 [B, H, Nq,  D]   queries
+ *   k, v   bf16 [B, H, Nkv, D]   keys, values
+ *   o_q    bf16 [B, H, Nq,  D]   OUT: sum_j quant(P)_ij v_j  (the returned output)
+ *   o_hp   bf16 [B, H, Nq,  D]   OUT: sum_j P_ij v_j         (straight-through output)
+ *   lse    fp32 [B, H, Nq]       OUT: m_i + log2(l_i) in base-2 units of the scaled
+ *                                logits s_ij * log2(e); kept for the backward.
+ *   sm_scale   finite, > 0; scores are s_ij = sm_scale * <q_i, k_j>.
+ *   causal     0 or 1; 1 masks keys j > i (top-left aligned); requires Nq == Nkv.
+ *   quant_mode QAT_QUANT_NONE or QAT_QUANT_P_FP8E4M3_ROW_TILE64.  Quantization:
+ *              per row i and tile t = {j : floor(j/64) = t}, amax = max_j p_ij,
+ *              code = E4M3_RNE_SATFINITE(p_ij * (448 / amax)),
+ *              quant(P)_ij = code * (amax / 448) / l_i, l_i summed from unquantized p.
+ *   D          64 or 128.   B, H, Nq >= 0 (any zero: nothing to do, returns QAT_OK);
+ *              Nkv >= 1 whenever there is work.
+ * Errors: QAT_ERR_INVALID_ARG (null or non-16-byte-aligned pointer, negative size,
+ *   Nkv < 1, D not in {64, 128}, bad sm_scale / causal / quant_mode, or a tensor of
+ *   more than 2^31 rows), QAT_ERR_UNSUPPORTED (causal with Nq != Nkv),
+ *   QAT_ERR_CUDA (launch failure).
+ */
+QAT_API qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v,
+                          void* o_q, void* o_hp, float* lse,
+                          int B, int H, int Nq, int Nkv, int D,
+                          float sm_scale, int causal, int quant_mode,
+                          void* stream);
+
+/*
+ * qat_attn_bwd_workspace_bytes -- device workspace qat_attn_bwd needs for these sizes
+ * (fp32 Delta [B, H, Nq] and scratch, 256-byte aligned pieces).  Returns 0 for
+ * invalid sizes.  Host-only; never touches the device.
+ */
+QAT_API size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D);
+
+/*
+ * qat_attn_bwd -- backward pass through the straight-through estimator: gradients of
+ * L = <dO, O_hp>, i.e. quantization of P is treated as the identity.
+ *   ("attn_qat_train.py", _attn_bwd_preprocess, _attn_bwd_dkdv, _attn_bwd_dq.)
+ *
+ *   q, k, v  bf16        the forward's inputs
+ *   o_hp     bf16 [B, H, Nq, D]  the forward's straight-through output
+ *   lse      fp32 [B, H, Nq]     the forward's lse output
+ *   dO       bf16 [B, H, Nq, D]  upstream gradient of o_q
+ *   dq       bf16 [B, H, Nq, D]  OUT
+ *   dk, dv   bf16 [B, H, Nkv, D] OUT
+ *   Delta_i = sum_d dO_id O_hp,id;  P_ij = exp2(s_ij log2(e) - lse_i);
+ *   dP = dO V^T;  dS = P o (dP - Delta);  dQ = sm_scale dS K;  dK = sm_scale dS^T Q;
+ *   dV = P^T dO.
+ *   quant_mode is validated but does not change the result (straight-through).
+ *   workspace  device buffer of at least qat_attn_bwd_workspace_bytes(...) bytes,
+ *              256-byte aligned, owned by the caller; its contents on entry are
+ *              ignored and on exit unspecified.
+ * Errors: as qat_attn_fwd, plus QAT_ERR_WORKSPACE when workspace is NULL or
+ *   workspace_bytes is too small.  Nq == 0 with Nkv >= 1 writes zero dk, dv.
+ */
+QAT_API qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v,
+                          const void* o_hp, const float* lse, const void* dO,
+                          void* dq, void* dk, void* dv,
+                          int B, int H, int Nq, int Nkv, int D,
+                          float sm_scale, int causal, int quant_mode,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+QAT_API const char* qat_status_string(qat_status_t status);
+
+/*
+ * qat_attn_device_status -- synchronizes `stream`, then reads and clears the
+ * library's device-side error word on the current device.  Kernels whose waits are
+ * bounded set it when a wait expires (they then return early instead of hanging).
+ * Returns QAT_OK, QAT_ERR_TIMEOUT, or QAT_ERR_CUDA if the synchronization failed.
+ */
+QAT_API qat_status_t qat_attn_device_status(void* stream);
+
+/*
+ * qat_debug_quant_tiles -- test entry: applies the kernels' own per-tile FP8 rule to
+ * given fp32 data.  ("attn_qat_train.py", fake_quantize call in _attn_fwd_inner.)
+ *   p       fp32 [rows, cols]  device, row-major; each row is split into tiles of 64
+ *                              columns aligned at column 0 (the last may be shorter)
+ *   deq     fp32 [rows, cols]  OUT: bf16-rounded quantized values, widened to fp32
+ *   scales  fp32 [rows, ceil(cols/64)]  OUT: amax / 448 (0 for an all-zero tile)
+ *   codes   u8   [rows, cols]  OUT: E4M3 code bytes
+ * Inputs must be finite and >= 0 (probabilities).  rows, cols >= 0.
+ * Errors: QAT_ERR_INVALID_ARG (null pointer with work to do, negative size).
+ */
+QAT_API qat_status_t qat_debug_quant_tiles(const float* p, int rows, int cols, float* deq,
+                                   float* scales, unsigned char* codes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QAT_ATTN_H */

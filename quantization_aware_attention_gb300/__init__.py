@@ -1,1 +1,11 @@
-"""GB300-native quantization-aware attention (QAT attention)."""
+"""GB300-native (sm_103a) quantization-aware attention (QAT attention).
+
+The computation lives in the C-ABI library ``libqat_attn.so`` (hand-written CUDA);
+``capi`` binds it with ctypes and ``attention`` wraps it for torch tensors and
+autograd.  Importing this package does not load the library; the first call does,
+and fails loudly if it has not been built.
+"""
+
+from .capi import QUANT_NONE, QUANT_P_FP8E4M3_ROW_TILE64, QatError, Status  # noqa: F401
+from .attention import (QATAttention, attention, qat_attention_backward,  # noqa: F401
+                        qat_attention_forward)

@@ -1,0 +1,111 @@
+"""Torch-facing API over the C ABI: output allocation, the backward workspace and the
+autograd Function.  torch supplies device memory and streams only; every step of the
+computation runs in the library's CUDA kernels.
+
+``attention(q, k, v, causal, sm_scale, quant_mode)`` returns the quantized output O_q
+and, under autograd, back-propagates through the straight-through estimator: the
+saved O_hp and log-sum-exp let the backward rematerialize P ("support for pytorch
+autograd": rematerialization as in FlashAttention; "attn_qat_train.py",
+_attention.forward saves q, k, v, O and M).
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import capi
+
+
+def _check(t: torch.Tensor, name: str, shape=None, dtype=torch.bfloat16) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, D]")
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    _check(q, "q")
+    _check(k, "k", (B, H, Nkv, D))
+    _check(v, "v", (B, H, Nkv, D))
+    return B, H, Nq, Nkv, D
+
+
+def _raise(st: capi.Status, what: str) -> None:
+    if st != capi.Status.OK:
+        raise capi.QatError(st, what)
+
+
+def qat_attention_forward(q, k, v, causal: bool = False, sm_scale: float | None = None,
+                          quant_mode: int = capi.QUANT_P_FP8E4M3_ROW_TILE64):
+    """Returns (o_q, o_hp, lse): bf16 [B,H,Nq,D], bf16 [B,H,Nq,D], fp32 [B,H,Nq] (base 2)."""
+    B, H, Nq, Nkv, D = _dims(q, k, v)
+    sm_scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    o_q = torch.empty_like(q)
+    o_hp = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = capi.qat_attn_fwd(q, k, v, o_q, o_hp, lse, B, H, Nq, Nkv, D, sm_scale,
+                               int(causal), quant_mode)
+    _raise(st, "qat_attn_fwd")
+    return o_q, o_hp, lse
+
+
+def qat_attention_backward(q, k, v, o_hp, lse, do, causal: bool = False,
+                           sm_scale: float | None = None,
+                           quant_mode: int = capi.QUANT_P_FP8E4M3_ROW_TILE64,
+                           workspace: torch.Tensor | None = None):
+    """Returns (dq, dk, dv) of L = <dO, O_hp> (straight-through estimator)."""
+    B, H, Nq, Nkv, D = _dims(q, k, v)
+    _check(o_hp, "o_hp", (B, H, Nq, D))
+    _check(do, "do", (B, H, Nq, D))
+    _check(lse, "lse", (B, H, Nq), torch.float32)
+    sm_scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    ws_bytes = capi.qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    with torch.cuda.device(q.device):
+        st = capi.qat_attn_bwd(q, k, v, o_hp, lse, do, dq, dk, dv, B, H, Nq, Nkv, D, sm_scale,
+                               int(causal), quant_mode, workspace, workspace.numel())
+    _raise(st, "qat_attn_bwd")
+    return dq, dk, dv
+
+
+class QATAttention(torch.autograd.Function):
+    """Forward returns O_q; backward returns dq, dk, dv through the straight-through
+    estimator (gradients of O_hp)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal=False, sm_scale=None,
+                quant_mode=capi.QUANT_P_FP8E4M3_ROW_TILE64):
+        o_q, o_hp, lse = qat_attention_forward(q, k, v, causal, sm_scale, quant_mode)
+        ctx.save_for_backward(q, k, v, o_hp, lse)
+        ctx.causal, ctx.sm_scale, ctx.quant_mode = causal, sm_scale, quant_mode
+        return o_q
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o_hp, lse = ctx.saved_tensors
+        dq, dk, dv = qat_attention_backward(q, k, v, o_hp, lse, do.contiguous(), ctx.causal,
+                                            ctx.sm_scale, ctx.quant_mode)
+        return dq, dk, dv, None, None, None
+
+
+def attention(q, k, v, causal: bool = False, sm_scale: float | None = None,
+              quant_mode: int = capi.QUANT_P_FP8E4M3_ROW_TILE64):
+    """QAT attention: the quantized output O_q, differentiable (straight-through)."""
+    return QATAttention.apply(q, k, v, causal, sm_scale, quant_mode)

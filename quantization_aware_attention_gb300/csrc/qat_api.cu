@@ -1,0 +1,172 @@
+// qat_api.cu -- the C ABI declared in include/qat_attn.h: host-side validation, the
+// backward workspace layout, kernel launches on the caller's stream, status codes and
+// the device-side error word.  No entry point here allocates device memory.
+#include "qat_attn.h"
+#include "qat_internal.h"
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+namespace qat {
+
+// Set by kernels whose bounded waits expire; read and cleared by qat_attn_device_status.
+__device__ unsigned int g_device_error = 0u;
+
+cudaError_t read_and_clear_device_error(unsigned int* out, cudaStream_t s) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0u;
+  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace qat
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr size_t kAlign = 256;
+constexpr long long kMaxRows = 2147483647LL;  // rows of a [B*H*N, D] view
+constexpr int kMaxBH = 65535;                   // grid y dimension
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Checks shared by the forward and backward entry points.  Sets *empty when there is
+// no query work (B, H or Nq is zero).
+qat_status_t check_sizes(int B, int H, int Nq, int Nkv, int D, float sm_scale, int causal,
+                         int quant_mode, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || Nq < 0 || Nkv < 0) return QAT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return QAT_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !isfinite(sm_scale)) return QAT_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return QAT_ERR_INVALID_ARG;
+  if (quant_mode != QAT_QUANT_NONE && quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64)
+    return QAT_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) {
+    *empty = true;
+    return QAT_OK;
+  }
+  if (Nkv < 1) return QAT_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * Nq > kMaxRows || bh * Nkv > kMaxRows) return QAT_ERR_INVALID_ARG;
+  if (bh > kMaxBH) return QAT_ERR_UNSUPPORTED;
+  if (causal && Nq != Nkv) return QAT_ERR_UNSUPPORTED;
+  if (Nq == 0) *empty = true;
+  return QAT_OK;
+}
+
+qat_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QAT_OK : QAT_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* qat_status_string(qat_status_t status) {
+  switch (status) {
+    case QAT_OK: return "QAT_OK";
+    case QAT_ERR_INVALID_ARG: return "QAT_ERR_INVALID_ARG: invalid argument";
+    case QAT_ERR_UNSUPPORTED: return "QAT_ERR_UNSUPPORTED: unsupported configuration";
+    case QAT_ERR_CUDA: return "QAT_ERR_CUDA: CUDA runtime or launch error";
+    case QAT_ERR_TIMEOUT: return "QAT_ERR_TIMEOUT: a bounded device wait expired";
+    case QAT_ERR_WORKSPACE: return "QAT_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "QAT_ERR_UNKNOWN: unknown status code";
+}
+
+qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v, void* o_q, void* o_hp,
+                          float* lse, int B, int H, int Nq, int Nkv, int D, float sm_scale,
+                          int causal, int quant_mode, void* stream) {
+  bool empty = false;
+  const qat_status_t st = check_sizes(B, H, Nq, Nkv, D, sm_scale, causal, quant_mode, &empty);
+  if (st != QAT_OK || empty) return st;
+  const void* ptrs[] = {q, k, v, o_q, o_hp, lse};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return QAT_ERR_INVALID_ARG;
+  qat::FwdArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.o_q = static_cast<uint16_t*>(o_q);
+  a.o_hp = static_cast<uint16_t*>(o_hp);
+  a.lse = lse;
+  a.B = B; a.H = H; a.Nq = Nq; a.Nkv = Nkv; a.D = D;
+  a.sm_scale = sm_scale;
+  a.qk_scale = sm_scale * kLog2e;
+  a.causal = causal;
+  a.quant = quant_mode == QAT_QUANT_P_FP8E4M3_ROW_TILE64;
+  return from_cuda(qat::launch_fwd_mma(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D) {
+  bool empty = false;
+  if (check_sizes(B, H, Nq, Nkv, D, 1.0f, 0, 0, &empty) != QAT_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
+  return round_up(rows * sizeof(float) > 0 ? rows * sizeof(float) : 1);
+}
+
+qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const void* o_hp,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          int B, int H, int Nq, int Nkv, int D, float sm_scale, int causal,
+                          int quant_mode, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  bool empty = false;
+  const qat_status_t st = check_sizes(B, H, Nq, Nkv, D, sm_scale, causal, quant_mode, &empty);
+  if (st != QAT_OK) return st;
+  if (B == 0 || H == 0) return QAT_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t kv_bytes = static_cast<size_t>(B) * H * Nkv * D * sizeof(uint16_t);
+  if (Nq == 0) {  // no queries: every key gets zero gradient
+    if (dk == nullptr || dv == nullptr || !aligned16(dk) || !aligned16(dv))
+      return QAT_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, s);
+    return from_cuda(e);
+  }
+  const void* ptrs[] = {q, k, v, o_hp, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return QAT_ERR_INVALID_ARG;
+  const size_t need = qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D);
+  if (workspace == nullptr || workspace_bytes < need) return QAT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return QAT_ERR_INVALID_ARG;
+
+  qat::BwdArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.o_hp = static_cast<const uint16_t*>(o_hp);
+  a.lse = lse;
+  a.dO = static_cast<const uint16_t*>(dO);
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.delta = static_cast<float*>(workspace);
+  a.B = B; a.H = H; a.Nq = Nq; a.Nkv = Nkv; a.D = D;
+  a.sm_scale = sm_scale;
+  a.qk_scale = sm_scale * kLog2e;
+  a.causal = causal;
+  cudaError_t e = qat::launch_bwd_preprocess(a, s);
+  if (e == cudaSuccess) e = qat::launch_bwd_mma(a, s);
+  return from_cuda(e);
+}
+
+qat_status_t qat_attn_device_status(void* stream) {
+  unsigned int word = 0u;
+  const cudaError_t e = qat::read_and_clear_device_error(&word, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return QAT_ERR_CUDA;
+  return word ? QAT_ERR_TIMEOUT : QAT_OK;
+}
+
+qat_status_t qat_debug_quant_tiles(const float* p, int rows, int cols, float* deq, float* scales,
+                                   unsigned char* codes, void* stream) {
+  if (rows < 0 || cols < 0) return QAT_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return QAT_OK;
+  if (p == nullptr || deq == nullptr || scales == nullptr || codes == nullptr)
+    return QAT_ERR_INVALID_ARG;
+  return from_cuda(qat::launch_debug_quant(p, rows, cols, deq, scales, codes,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared symbol, and its
+host-side validation rejects bad arguments before anything reaches a device.
+Every call here fails validation (or has no work), so nothing is ever launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantization_aware_attention_gb300 import build as qbuild
+from quantization_aware_attention_gb300 import capi
+from quantization_aware_attention_gb300.capi import Status
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "qat_attn.h")
+A = 0x100000  # a 256-byte-aligned fake address: never dereferenced by these tests
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    qbuild.build()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(qat_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert names == sorted(capi.EXPORTED)
+    L = ctypes.CDLL(capi.LIB_PATH)
+    for n in names:
+        assert getattr(L, n) is not None
+
+
+def test_status_strings():
+    for s in Status:
+        assert capi.qat_status_string(s).startswith("QAT_")
+    assert "UNKNOWN" in capi.qat_status_string(99)
+
+
+def fwd(**kw):
+    args = dict(q=A, k=A, v=A, o_q=A, o_hp=A, lse=A, B=1, H=1, Nq=8, Nkv=8, D=64,
+                sm_scale=0.125, causal=0, quant_mode=1, stream=0)
+    args.update(kw)
+    return capi.qat_attn_fwd(**args)
+
+
+def bwd(**kw):
+    args = dict(q=A, k=A, v=A, o_hp=A, lse=A, dO=A, dq=A, dk=A, dv=A, B=1, H=1, Nq=8, Nkv=8,
+                D=64, sm_scale=0.125, causal=0, quant_mode=1, workspace=None,
+                workspace_bytes=0, stream=0)
+    args.update(kw)
+    return capi.qat_attn_bwd(**args)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(D=96), Status.INVALID_ARG),
+    (dict(D=256), Status.INVALID_ARG),
+    (dict(B=-1), Status.INVALID_ARG),
+    (dict(Nkv=0), Status.INVALID_ARG),
+    (dict(sm_scale=0.0), Status.INVALID_ARG),
+    (dict(sm_scale=float("nan")), Status.INVALID_ARG),
+    (dict(sm_scale=float("inf")), Status.INVALID_ARG),
+    (dict(causal=2), Status.INVALID_ARG),
+    (dict(quant_mode=7), Status.INVALID_ARG),
+    (dict(q=None), Status.INVALID_ARG),
+    (dict(lse=None), Status.INVALID_ARG),
+    (dict(o_hp=A + 8), Status.INVALID_ARG),
+    (dict(causal=1, Nkv=9), Status.UNSUPPORTED),
+    (dict(B=70000), Status.UNSUPPORTED),
+    (dict(B=65536, H=65536, Nq=1, Nkv=1), Status.INVALID_ARG),
+    (dict(B=0, q=None, k=None), Status.OK),
+    (dict(Nq=0, q=None), Status.OK),
+])
+def test_forward_validation(kw, want):
+    assert fwd(**kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(D=32), Status.INVALID_ARG),
+    (dict(dq=None), Status.INVALID_ARG),
+    (dict(dO=A + 4), Status.INVALID_ARG),
+    (dict(workspace=None, workspace_bytes=0), Status.WORKSPACE),
+    (dict(workspace=A, workspace_bytes=16), Status.WORKSPACE),
+    (dict(workspace=A + 16, workspace_bytes=1 << 20), Status.INVALID_ARG),
+    (dict(causal=1, Nq=16), Status.UNSUPPORTED),
+    (dict(quant_mode=3), Status.INVALID_ARG),
+    (dict(H=0, q=None), Status.OK),
+    (dict(Nq=0, dk=None), Status.INVALID_ARG),
+])
+def test_backward_validation(kw, want):
+    assert bwd(**kw) == want
+
+
+def test_workspace_bytes():
+    assert capi.qat_attn_bwd_workspace_bytes(1, 40, 32768, 32768, 128) >= 40 * 32768 * 4
+    assert capi.qat_attn_bwd_workspace_bytes(2, 4, 8, 8, 64) % 256 == 0
+    assert capi.qat_attn_bwd_workspace_bytes(1, 1, 8, 8, 96) == 0
+    assert capi.qat_attn_bwd_workspace_bytes(-1, 1, 8, 8, 64) == 0
+
+
+def test_debug_quant_validation():
+    assert capi.qat_debug_quant_tiles(None, -1, 4, A, A, A, stream=0) == Status.INVALID_ARG
+    assert capi.qat_debug_quant_tiles(None, 4, 64, A, A, A, stream=0) == Status.INVALID_ARG
+    assert capi.qat_debug_quant_tiles(None, 0, 64, None, None, None, stream=0) == Status.OK

@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
+seeded inputs.  Full tensors where the oracle finishes in seconds; sampled heads, rows
+and keys at the full workload sizes."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import qat_oracle as orc
+from quantization_aware_attention_gb300 import build as qbuild
+from quantization_aware_attention_gb300 import capi
+from quantization_aware_attention_gb300.attention import (qat_attention_backward,
+                                                          qat_attention_forward)
+from quantization_aware_attention_gb300.capi import Status
+from quantization_aware_attention_gb300.inputs import WORKLOADS, custom_inputs, make_inputs
+
+from gpu_util import TOL_HP, TOL_Q, dev_bf16, host_f64, oracle_f64, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    qbuild.build()
+
+
+def run_gpu(inp, causal, sm_scale, quant=1):
+    q, k, v, do = (dev_bf16(inp[n]) for n in ("q", "k", "v", "do"))
+    o_q, o_hp, lse = qat_attention_forward(q, k, v, causal, sm_scale, quant)
+    dq, dk, dv = qat_attention_backward(q, k, v, o_hp, lse, do, causal, sm_scale, quant)
+    torch.cuda.synchronize()
+    assert capi.qat_attn_device_status() == Status.OK
+    return dict(o_q=o_q, o_hp=o_hp, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def check_full(inp, causal, sm_scale, heads=None):
+    """Compare every output of the listed (b, h) heads (default all) with the oracle."""
+    g = run_gpu(inp, causal, sm_scale)
+    f = oracle_f64(inp)
+    B, H = inp["q"].shape[:2]
+    heads = heads or [(b, h) for b in range(B) for h in range(H)]
+    want = {n: [] for n in ("o_q", "o_hp", "lse", "dq", "dk", "dv")}
+    got = {n: [] for n in want}
+    for b, h in heads:
+        r = orc.head_forward(f["q"][b, h], f["k"][b, h], f["v"][b, h], sm_scale, causal, True)
+        dq, dk, dv = orc.head_backward(f["q"][b, h], f["k"][b, h], f["v"][b, h], f["do"][b, h],
+                                       sm_scale, causal)
+        for n, val in (("o_q", r["o_q"]), ("o_hp", r["o_hp"]), ("lse", r["lse"]),
+                       ("dq", dq), ("dk", dk), ("dv", dv)):
+            want[n].append(val)
+            got[n].append(host_f64(g[n][b, h]))
+    errs = {n: rel_l2(np.stack(got[n]), np.stack(want[n])) for n in want}
+    lse_abs = float(np.max(np.abs(np.stack(got["lse"]) - np.stack(want["lse"]))))
+    assert errs["o_hp"] <= TOL_HP and errs["lse"] <= TOL_HP, errs
+    assert lse_abs < 1e-3, lse_abs
+    for n in ("o_q", "dq", "dk", "dv"):
+        assert errs[n] <= TOL_Q, (n, errs)
+    # O_q really is quantized: it differs from O_hp by the FP8 error, not by zero
+    assert rel_l2(np.stack(got["o_q"]), np.stack(got["o_hp"])) > 1e-4
+    return errs
+
+
+# ------------------------------------------------------------------ quant primitive
+
+def test_quant_primitive_bit_exact():
+    rng = np.random.default_rng(11)
+    rows, cols = 3000, 200                          # 3 full tiles + a ragged tile of 8
+    p = np.exp(rng.standard_normal((rows, cols)) * 4).astype(np.float32)
+    p[0] = 0.0                                      # all-zero tiles
+    p[1, 64:128] = 0.0
+    p[2] *= np.float32(1e-36)                       # tiny (some subnormal) values
+    p[3] = np.float32(1.0)
+    p[4, :] = np.float32(2.0 ** -20)
+    p[5] = np.minimum(p[5], np.float32(1e30))
+    tiles = (cols + 63) // 64
+    dp = torch.from_numpy(p).cuda()
+    deq = torch.empty_like(dp)
+    scales = torch.empty((rows, tiles), dtype=torch.float32, device="cuda")
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    assert capi.qat_debug_quant_tiles(dp, rows, cols, deq, scales, codes) == Status.OK
+    torch.cuda.synchronize()
+    deq, scales, codes = deq.cpu().numpy(), scales.cpu().numpy(), codes.cpu().numpy()
+    for t in range(tiles):
+        sl = slice(t * 64, min(cols, (t + 1) * 64))
+        w_deq, w_scale, w_codes = orc.quant_tiles_fp32(p[:, sl])
+        assert np.array_equal(codes[:, sl], w_codes), t
+        assert np.array_equal(scales[:, t].view(np.uint32), w_scale.view(np.uint32)), t
+        assert np.array_equal(deq[:, sl].view(np.uint32), w_deq.view(np.uint32)), t
+
+
+# ------------------------------------------------------------------ workloads
+
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_small_workloads_full(name):
+    w = WORKLOADS[name]
+    check_full(make_inputs(w), w.causal, w.sm_scale)
+
+
+def test_c3_dit_outlier_channels_sampled_heads():
+    w = WORKLOADS["c3"]
+    check_full(make_inputs(w), w.causal, w.sm_scale, heads=[(0, 0), (0, 13), (0, 23)])
+
+
+def test_c5b_cross_attention_sampled_heads():
+    w = WORKLOADS["c5b"]
+    check_full(make_inputs(w), w.causal, w.sm_scale, heads=[(0, 0), (0, 39)])
+
+
+@pytest.mark.parametrize("B,H,Nq,Nkv,D,causal", [
+    (1, 1, 1, 1, 64, False),
+    (1, 1, 1, 1, 128, True),
+    (1, 2, 63, 63, 128, True),
+    (1, 1, 65, 65, 64, True),
+    (1, 1, 129, 129, 128, False),
+    (1, 1, 129, 200, 128, False),
+    (2, 1, 100, 37, 64, False),
+    (1, 1, 200, 200, 128, True),
+    (1, 1, 7, 300, 128, False),
+])
+def test_edge_shapes(B, H, Nq, Nkv, D, causal):
+    inp = custom_inputs(500 + Nq + Nkv, B, H, Nq, Nkv, D)
+    check_full(inp, causal, 1.0 / np.sqrt(D))
+
+
+def test_large_scale_and_quant_off():
+    inp = custom_inputs(77, 1, 2, 130, 130, 128)
+    check_full(inp, False, 0.5)  # sharper softmax: many tiles with tiny amax
+    q, k, v = (dev_bf16(inp[n]) for n in ("q", "k", "v"))
+    o_q, o_hp, _ = qat_attention_forward(q, k, v, False, 0.5, capi.QUANT_NONE)
+    assert torch.equal(o_q, o_hp)
+
+
+def test_backward_without_queries_zeroes_key_grads():
+    k = torch.randn(1, 2, 70, 64, device="cuda").to(torch.bfloat16)
+    q = torch.empty(1, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(1, 2, 0, device="cuda")
+    dk = torch.full_like(k, 3.0)
+    dv = torch.full_like(k, 3.0)
+    st = capi.qat_attn_bwd(q, k, k, q, lse, q, q, dk, dv, 1, 2, 0, 70, 64, 0.125, 0, 1, None, 0)
+    torch.cuda.synchronize()
+    assert st == Status.OK and not dk.any() and not dv.any()
+
+
+def test_deterministic():
+    inp = custom_inputs(91, 1, 2, 300, 300, 128)
+    a = run_gpu(inp, False, 0.088)
+    b = run_gpu(inp, False, 0.088)
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+
+
+# ------------------------------------------------------------------ full-size, sampled
+
+def _sampled_full_size(name, fwd_heads, bwd_head, n_rows=256, n_keys=64):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    g = run_gpu(inp, w.causal, w.sm_scale)
+    rng = np.random.default_rng(w.idx)
+    f = oracle_f64(inp)
+    got, want = {n: [] for n in ("o_q", "o_hp", "lse")}, {n: [] for n in ("o_q", "o_hp", "lse")}
+    for b, h in fwd_heads:
+        rows = np.sort(rng.choice(w.Nq, n_rows, replace=False))
+        r = orc.head_forward(f["q"][b, h], f["k"][b, h], f["v"][b, h], w.sm_scale, w.causal,
+                             True, rows=rows)
+        for n in got:
+            got[n].append(host_f64(g[n][b, h])[rows])
+            want[n].append(r[n])
+    e = {n: rel_l2(np.concatenate(got[n]), np.concatenate(want[n])) for n in got}
+    assert e["o_hp"] <= TOL_HP and e["lse"] <= TOL_HP and e["o_q"] <= TOL_Q, e
+    b, h = bwd_head
+    rows = np.sort(rng.choice(w.Nq, n_rows, replace=False))
+    keys = np.sort(rng.choice(w.Nkv, n_keys, replace=False))
+    dq, dk, dv = orc.head_backward_sampled(f["q"][b, h], f["k"][b, h], f["v"][b, h],
+                                           f["do"][b, h], w.sm_scale, w.causal, rows, keys)
+    eb = {"dq": rel_l2(host_f64(g["dq"][b, h])[rows], dq),
+          "dk": rel_l2(host_f64(g["dk"][b, h])[keys], dk),
+          "dv": rel_l2(host_f64(g["dv"][b, h])[keys], dv)}
+    assert all(x <= TOL_Q for x in eb.values()), eb
+    for n in ("o_q", "dq", "dk", "dv"):
+        assert torch.isfinite(g[n]).all(), n
+
+
+def test_c4_video_dit_full_size_sampled():
+    _sampled_full_size("c4", fwd_heads=[(0, 0), (0, 17), (0, 39)], bwd_head=(0, 21))
+
+
+def test_c5a_causal_full_size_sampled():
+    _sampled_full_size("c5a", fwd_heads=[(0, 0), (3, 31)], bwd_head=(2, 5))
