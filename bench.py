@@ -351,13 +351,17 @@ def run_ours(args, w):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows = 2048
-        tf, dt, _ = oracle_sample_tflops(w, rows)
+        rows, chunks = 2048, 4
+        secs, flops = 0.0, 0.0
+        for c in range(chunks):
+            _, dt, pairs = oracle_sample_tflops(w, rows, seed=c)
+            secs += dt
+            flops += 16.0 * pairs * w.D
         line["cpu_baseline"] = {
-            "value": tf, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": (f"one head of {w.name}: {rows} query rows x {w.Nkv} keys, fp64 forward "
-                       f"(with FP8 quantization) + backward, {dt:.1f} s; numpy BLAS matmuls, "
-                       f"elementwise steps single-threaded")}
+            "value": flops / secs / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"one head of {w.name}: {chunks} x {rows} query rows x {w.Nkv} keys, fp64 "
+                       f"forward (with FP8 quantization) + backward, {secs:.1f} s; numpy BLAS "
+                       f"matmuls, elementwise steps single-threaded")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -55,8 +55,11 @@ def check_full(inp, causal, sm_scale, heads=None):
     assert lse_abs < 1e-3, lse_abs
     for n in ("o_q", "dq", "dk", "dv"):
         assert errs[n] <= TOL_Q, (n, errs)
-    # O_q really is quantized: it differs from O_hp by the FP8 error, not by zero
-    assert rel_l2(np.stack(got["o_q"]), np.stack(got["o_hp"])) > 1e-4
+    # O_q really is quantized: with more than a few keys per row it differs from O_hp
+    # by the FP8 error (with one key P = 1 quantizes exactly and the two are equal)
+    if inp["k"].shape[2] >= 16:
+        assert rel_l2(np.stack(got["o_q"]), np.stack(got["o_hp"])) > 1e-4
+    print("errors", {n: f"{e:.2e}" for n, e in errs.items()})
     return errs
 
 
