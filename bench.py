@@ -91,6 +91,9 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        t0 = time.time()  # let nvidia-smi start up before the timed region begins
+        while not self.lines and time.time() - t0 < 10.0:
+            time.sleep(0.05)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -263,8 +266,8 @@ def run_ours(args, w):
     clocks = ClockSampler(local)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
     clocks.start()
+    barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
