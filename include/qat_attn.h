@@ -123,6 +123,29 @@ QAT_API qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v,
                           float sm_scale, int causal, int quant_mode,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * qat_attn_bwd_noalloc -- the same backward as qat_attn_bwd for callers that cannot
+ * allocate device memory: for example a program whose device memory all belongs to
+ * another runtime's pool, or one that must not allocate once running (an allocation
+ * can block on the device or fail under memory pressure mid-step).  The paper has no
+ * counterpart; this entry exists for such callers only.
+ *   Arguments as qat_attn_bwd, without workspace / workspace_bytes.  The scratch lives
+ *   in a fixed 32 MiB device array inside the library, held on every GPU that loads
+ *   the library until the process exits.  It allocates nothing (no cudaMalloc,
+ *   cudaFree or allocating library call).
+ *   The first call on a device looks up that array's device address with the device
+ *   current; make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents; calls that overlap
+ *   on the GPU race on it and must be ordered by the caller.
+ * Errors: as qat_attn_bwd; QAT_ERR_WORKSPACE when the sizes need more scratch than the
+ *   array holds (qat_attn_bwd_workspace_bytes(...) > 32 MiB).
+ */
+QAT_API qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const void* v,
+                          const void* o_hp, const float* lse, const void* dO,
+                          void* dq, void* dk, void* dv,
+                          int B, int H, int Nq, int Nkv, int D,
+                          float sm_scale, int causal, int quant_mode, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 QAT_API const char* qat_status_string(qat_status_t status);
 

@@ -21,6 +21,7 @@ EXPORTED = (
     "qat_attn_fwd",
     "qat_attn_bwd_workspace_bytes",
     "qat_attn_bwd",
+    "qat_attn_bwd_noalloc",
     "qat_status_string",
     "qat_attn_device_status",
     "qat_debug_quant_tiles",
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.qat_attn_bwd_workspace_bytes.restype = _sz
         L.qat_attn_bwd.argtypes = [_vp] * 9 + [_i] * 5 + [_f, _i, _i, _vp, _sz, _vp]
         L.qat_attn_bwd.restype = _i
+        L.qat_attn_bwd_noalloc.argtypes = [_vp] * 9 + [_i] * 5 + [_f, _i, _i, _vp]
+        L.qat_attn_bwd_noalloc.restype = _i
         L.qat_status_string.argtypes = [_i]
         L.qat_status_string.restype = ctypes.c_char_p
         L.qat_attn_device_status.argtypes = [_vp]
@@ -113,6 +116,14 @@ def qat_attn_bwd(q, k, v, o_hp, lse, dO, dq, dk, dv, B, H, Nq, Nkv, D, sm_scale,
                                      _ptr(dq), _ptr(dk), _ptr(dv), B, H, Nq, Nkv, D,
                                      float(sm_scale), int(causal), int(quant_mode),
                                      _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def qat_attn_bwd_noalloc(q, k, v, o_hp, lse, dO, dq, dk, dv, B, H, Nq, Nkv, D, sm_scale, causal,
+                         quant_mode, stream=None) -> Status:
+    return Status(lib().qat_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o_hp), _ptr(lse),
+                                             _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Nq,
+                                             Nkv, D, float(sm_scale), int(causal),
+                                             int(quant_mode), _stream(stream)))
 
 
 def qat_attn_device_status(stream=None) -> Status:
