@@ -1,0 +1,488 @@
+// attn_fwd_sm100.cu -- QAT attention forward on the Blackwell tensor core (tcgen05 +
+// TMEM + TMA), warp-specialized and persistent.
+//
+// Method ("attn_qat_train.py", _attn_fwd / _attn_fwd_inner), per query row i and KV
+// tile j:  S = Q K_j^T;  x = S * qk_scale (masked keys -inf);  running max m;
+//   p = exp2(x - m);  l = alpha l + rowsum p (unquantized);  per 64-key quant tile
+//   amax = max p, Pq = quant(p) (qat_quant.cuh);  O_q = alpha O_q + Pq V_j;
+//   O_hp = alpha O_hp + P V_j;  epilogue O / l, lse = m + log2 l.
+//
+// CTA layout (192 threads, one CTA per SM, persistent over (head, 128-row q tile)):
+//   warp 0      TMA producer: Q tile once per work item, K tiles (3-stage ring) and
+//               V tiles (2-stage ring), 128 keys x D, 128-byte swizzled boxes.
+//   warp 1      TMEM allocator; lane 0 issues every tcgen05.mma:
+//                 S_j = Q K_j^T            (SS, M=128, N=128 keys, K=D) -> TMEM S[j%2]
+//                 O_q += Pq_j V_j          (TS: A = Pq in TMEM, B = V MN-major in smem)
+//                 O_hp += P_j V_j          (TS, same V descriptors: the two P tiles share V)
+//               issue order S_j, PV_{j-1}, S_{j+1}, ... so the tensor core computes the
+//               next scores while the softmax warps work on the current tile.
+//   warps 2-5   softmax + quantization, one thread per query row (TMEM lane), then the
+//               epilogue.  P is written back into the S buffer it came from as two bf16
+//               tiles (Pq in columns 0-63, P in 64-127), consumed by the TS MMAs.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O_q [256,256+D), O_hp [256+D,256+2D).
+//
+// The running max is updated only when it grows by more than 8 (base-2 units), so P
+// may reach 2^8 and the O rescale is rare.  The FP8 code depends only on p / amax, so
+// this leaves the quantization unchanged in exact arithmetic (the max element of every
+// tile still maps to 448) and l, O_q and O_hp stay consistent.
+#include "qat_internal.h"
+#include "qat_quant.cuh"
+#include "sm100.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+namespace qat {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+
+template <int D>
+struct FwdTc {
+  static constexpr int kChunks = D / 64;                 // 128-byte column chunks per row
+  static constexpr uint32_t kChunkBytes = kBM * 128;     // one 128-row x 64-col box: 16 KB
+  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + kTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr uint32_t kOffMisc = kOffBar + 256;
+  static constexpr uint32_t kUsed = kOffMisc + 64;
+  // at least 116 KB so that no two CTAs share an SM (each holds all 512 TMEM columns)
+  static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
+  static constexpr uint32_t kTmemOq = 256;
+  static constexpr uint32_t kTmemOhp = 256 + D;
+};
+
+// barrier indices (8 bytes each) in the barrier block
+enum : uint32_t {
+  BAR_Q_FULL = 0, BAR_Q_EMPTY = 1, BAR_K_FULL = 2, BAR_K_EMPTY = 5, BAR_V_FULL = 8,
+  BAR_V_EMPTY = 10, BAR_S_FULL = 12, BAR_P_FULL = 14, BAR_O_DONE = 16, BAR_O_EMPTY = 17,
+  BAR_DRAIN = 18, BAR_COUNT = 19
+};
+
+struct TcParams {
+  FwdArgs a;
+  unsigned int* err;
+  int mtiles;   // ceil(Nq / 128)
+  int items;    // B * H * mtiles
+};
+
+__device__ __forceinline__ void item_coords(int idx, const TcParams& p, int& bh, int& mt) {
+  const int BH = p.a.B * p.a.H;
+  if (p.a.causal) {  // longest rows first
+    mt = p.mtiles - 1 - idx / BH;
+    bh = idx % BH;
+  } else {           // head-major: CTAs running together share one head's K/V in L2
+    bh = idx / p.mtiles;
+    mt = idx % p.mtiles;
+  }
+}
+
+__device__ __forceinline__ int kv_tiles(const TcParams& p, int mt) {
+  const int n = (p.a.Nkv + kBN - 1) / kBN;
+  return p.a.causal ? min(n, mt + 1) : n;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+  using C = FwdTc<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + C::kOffBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 8);
+  auto bar = [&](uint32_t i) { return bars + 8u * i; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(BAR_Q_FULL), 1);
+    mbar_init(bar(BAR_Q_EMPTY), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(bar(BAR_K_FULL + s), 1);
+      mbar_init(bar(BAR_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(bar(BAR_V_FULL + s), 1);
+      mbar_init(bar(BAR_V_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(BAR_S_FULL + b), 1);
+      mbar_init(bar(BAR_P_FULL + b), 128);
+    }
+    mbar_init(bar(BAR_O_DONE), 1);
+    mbar_init(bar(BAR_O_EMPTY), 128);
+    mbar_init(bar(BAR_DRAIN), 1);
+    fence_barrier_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const int BH = p.a.B * p.a.H;
+  (void)BH;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kc = 0, vc = 0;
+      int it = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, mt;
+        item_coords(idx, p, bh, mt);
+        const int J = kv_tiles(p, mt);
+        ok = mbar_wait(bar(BAR_Q_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(BAR_Q_FULL), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(base + C::kOffQ + c * C::kChunkBytes, &tmQ, bar(BAR_Q_FULL), 64 * c,
+                      mt * kBM, bh);
+        for (int j = 0; j <= J && ok; ++j) {
+          if (j < J) {  // K_j
+            const uint32_t st = kc % kKStages, use = kc / kKStages;
+            ok = mbar_wait(bar(BAR_K_EMPTY + st), (use & 1) ^ 1, abort_flag, p.err);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(BAR_K_FULL + st), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(base + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes, &tmK,
+                          bar(BAR_K_FULL + st), 64 * c, j * kBN, bh);
+            ++kc;
+          }
+          if (j >= 1) {  // V_{j-1}: one tile behind K, matching the MMA issue order
+            const uint32_t st = vc % kVStages, use = vc / kVStages;
+            ok = mbar_wait(bar(BAR_V_EMPTY + st), (use & 1) ^ 1, abort_flag, p.err);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(BAR_V_FULL + st), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(base + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes, &tmV,
+                          bar(BAR_V_FULL + st), 64 * c, (j - 1) * kBN, bh);
+            ++vc;
+          }
+        }
+      }
+      // drain: every issued load must land before the CTA can exit
+      for (uint32_t i = (kc > kKStages ? kc - kKStages : 0); i < kc; ++i)
+        mbar_wait(bar(BAR_K_FULL + i % kKStages), (i / kKStages) & 1, abort_flag, p.err);
+      for (uint32_t i = (vc > kVStages ? vc - kVStages : 0); i < vc; ++i)
+        mbar_wait(bar(BAR_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, true);
+      uint32_t kc = 0, vc = 0, sc = 0, pc = 0;
+      int it = 0;
+      bool ok = true, issued = false;
+      auto issue_pv = [&](bool first) -> bool {
+        const uint32_t b = pc & 1;
+        if (!mbar_wait(bar(BAR_P_FULL + b), (pc >> 1) & 1, abort_flag, p.err)) return false;
+        if (first && !mbar_wait(bar(BAR_O_EMPTY), (it & 1) ^ 1, abort_flag, p.err)) return false;
+        const uint32_t st = vc % kVStages;
+        if (!mbar_wait(bar(BAR_V_FULL + st), (vc / kVStages) & 1, abort_flag, p.err))
+          return false;
+        tc_fence_after();
+        const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
+        const uint32_t sP = tbase + b * 128;
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t dv = smem_desc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
+          mma_ts(tbase + C::kTmemOq, sP + 8 * ks, dv, idPV, (!first || ks > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t dv = smem_desc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
+          mma_ts(tbase + C::kTmemOhp, sP + 64 + 8 * ks, dv, idPV, (!first || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(BAR_V_EMPTY + st));
+        mma_commit(bar(BAR_O_DONE));
+        ++vc;
+        ++pc;
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, mt;
+        item_coords(idx, p, bh, mt);
+        const int J = kv_tiles(p, mt);
+        ok = mbar_wait(bar(BAR_Q_FULL), it & 1, abort_flag, p.err);
+        for (int j = 0; j < J && ok; ++j) {
+          const uint32_t st = kc % kKStages;
+          ok = mbar_wait(bar(BAR_K_FULL + st), (kc / kKStages) & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t b = sc & 1;
+          const uint32_t qb = base + C::kOffQ;
+          const uint32_t kb = base + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+            mma_ss(tbase + b * 128, smem_desc_sw128(qb + off, 16, 1024),
+                   smem_desc_sw128(kb + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(bar(BAR_K_EMPTY + st));
+          mma_commit(bar(BAR_S_FULL + b));
+          if (j == J - 1) mma_commit(bar(BAR_Q_EMPTY));
+          ++kc;
+          ++sc;
+          if (j >= 1) ok = issue_pv(j == 1);
+        }
+        if (ok) ok = issue_pv(J == 1);
+      }
+      if (issued) {  // drain: wait until every MMA this thread issued has completed
+        mma_commit(bar(BAR_DRAIN));
+        mbar_wait(bar(BAR_DRAIN), 0, abort_flag, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    const int r = 32 * quarter + lane;            // row of the 128-row tile
+    const uint32_t lrow = (32u * quarter) << 16;  // TMEM lane offset
+    const float qk = p.a.qk_scale;
+    // tcgen05.ld/st are warp-collective: every wait result is made warp-uniform
+    auto wwait = [&](uint32_t b_, uint32_t par) {
+      const bool w = mbar_wait(b_, par, abort_flag, p.err);
+      return __all_sync(0xffffffffu, w) != 0;
+    };
+    uint32_t sc = 0, pvc = 0;                     // S tiles consumed, PV groups done
+    int it = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+      int bh, mt;
+      item_coords(idx, p, bh, mt);
+      const int J = kv_tiles(p, mt);
+      const int row = mt * kBM + r;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < J && ok; ++j) {
+        const uint32_t b = sc & 1;
+        ok = wwait(bar(BAR_S_FULL + b), (sc >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        const uint32_t tS = tbase + lrow + b * 128;
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_wait_ld();
+        float* s = reinterpret_cast<float*>(sr);
+        const int key0 = j * kBN;
+        if (key0 + kBN > p.a.Nkv || (p.a.causal && j == mt)) {
+          const int lim = p.a.causal ? min(p.a.Nkv - 1, row) : p.a.Nkv - 1;
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (key0 + i > lim) s[i] = -INFINITY;
+        }
+        float t0 = fmax3(s[0], s[1], s[2]), t1 = fmax3(s[64], s[65], s[66]);
+#pragma unroll
+        for (int i = 3; i < 63; i += 2) {
+          t0 = fmax3(t0, s[i], s[i + 1]);
+          t1 = fmax3(t1, s[64 + i], s[64 + i + 1]);
+        }
+        t0 = fmaxf(t0, s[63]);
+        t1 = fmaxf(t1, s[127]);
+        const float tmax = fmaxf(t0, t1) * qk;
+        float alpha = 1.f;
+        bool resc = false;
+        if (tmax > m_used + kRescaleThreshold) {
+          if (j > 0) {
+            resc = true;
+            alpha = ex2(m_used - tmax);
+          }
+          m_used = tmax;
+        }
+        const float negm = -m_used;
+        const TileScale ts0 = tile_scale(ex2(fmaf(t0, qk, negm)));
+        const TileScale ts1 = tile_scale(ex2(fmaf(t1, qk, negm)));
+        l *= alpha;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pq[16], ph[16];
+          const TileScale ts = c < 2 ? ts0 : ts1;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(s[32 * c + 2 * i], qk, negm));
+            const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], qk, negm));
+            l += p0 + p1;
+            ph[i] = pack_bf16(p0, p1);
+            if (p.a.quant) {
+              uint16_t cd;
+              __nv_bfloat162 qv = quant_pair(p0, p1, ts, &cd);
+              pq[i] = *reinterpret_cast<uint32_t*>(&qv);
+            } else {
+              pq[i] = ph[i];
+            }
+          }
+          tmem_st16(tS + 16 * c, pq);
+          tmem_st16(tS + 64 + 16 * c, ph);
+        }
+        tmem_wait_st();
+        if (__any_sync(0xffffffffu, resc)) {
+          // O must hold every PV issued so far before it is rescaled
+          ok = wwait(bar(BAR_O_DONE), (pvc - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t tO = tbase + lrow + (half ? C::kTmemOhp : C::kTmemOq);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + 32 * c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + 32 * c, o);
+            }
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(BAR_P_FULL + b));
+        ++sc;
+        ++pvc;  // PV_j will be issued once every row has arrived
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      ok = wwait(bar(BAR_O_DONE), (pvc - 1) & 1);
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const bool in = row < p.a.Nq;
+      const size_t orow = (static_cast<size_t>(bh) * p.a.Nq + (in ? row : 0)) * D;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t tO = tbase + lrow + (half ? C::kTmemOhp : C::kTmemOq);
+        uint16_t* out = half ? p.a.o_hp : p.a.o_q;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (in) {
+            uint4* dst = reinterpret_cast<uint4*>(out + orow + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(BAR_O_EMPTY));
+      if (in) p.a.lse[static_cast<size_t>(bh) * p.a.Nq + row] = m_used + log2f(l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); boxes of 64 x 128 x 1.
+bool make_map(CUtensorMap* m, const void* ptr, int D, int N, int BH) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(N) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_fwd_tc_d(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
+  using C = FwdTc<D>;
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, D, a.Nq, BH) || !make_map(&mk, a.k, D, a.Nkv, BH) ||
+      !make_map(&mv, a.v, D, a.Nkv, BH))
+    return cudaErrorInvalidValue;
+  TcParams p;
+  p.a = a;
+  p.err = err;
+  p.mtiles = (a.Nq + kBM - 1) / kBM;
+  p.items = BH * p.mtiles;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int grid = p.items < num_sms ? p.items : num_sms;
+  attn_fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
+  return a.D == 64 ? launch_fwd_tc_d<64>(a, err, num_sms, s)
+                   : launch_fwd_tc_d<128>(a, err, num_sms, s);
+}
+
+}  // namespace qat

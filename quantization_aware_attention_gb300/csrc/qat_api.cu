@@ -8,6 +8,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace qat {
 
 // Set by kernels whose bounded waits expire; read and cleared by qat_attn_device_status.
@@ -20,6 +22,34 @@ cudaError_t read_and_clear_device_error(unsigned int* out, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const unsigned int zero = 0u;
   return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_ctx_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t device_context(unsigned int** err, int* num_sms) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_ctx_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+    g_num_sms[dev] = n;
+  }
+  *err = g_err_ptr[dev];
+  *num_sms = g_num_sms[dev];
+  return cudaSuccess;
 }
 
 }  // namespace qat
@@ -97,7 +127,11 @@ qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v, void* o_q
   a.qk_scale = sm_scale * kLog2e;
   a.causal = causal;
   a.quant = quant_mode == QAT_QUANT_P_FP8E4M3_ROW_TILE64;
-  return from_cuda(qat::launch_fwd_mma(a, static_cast<cudaStream_t>(stream)));
+  unsigned int* err = nullptr;
+  int num_sms = 0;
+  cudaError_t e = qat::device_context(&err, &num_sms);
+  if (e == cudaSuccess) e = qat::launch_fwd_tc(a, err, num_sms, static_cast<cudaStream_t>(stream));
+  return from_cuda(e);
 }
 
 size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D) {

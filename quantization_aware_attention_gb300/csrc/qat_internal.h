@@ -41,7 +41,7 @@ struct BwdArgs {
 };
 
 // Kernel launchers (return cudaGetLastError() after the launches).
-cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_tc(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_mma(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_debug_quant(const float* p, int rows, int cols, float* deq,
@@ -49,5 +49,7 @@ cudaError_t launch_debug_quant(const float* p, int rows, int cols, float* deq,
 
 // Device-side error word (bounded waits set it); defined in qat_api.cu.
 cudaError_t read_and_clear_device_error(unsigned int* out, cudaStream_t s);
+// Device address of that word and the SM count, for the current device (cached).
+cudaError_t device_context(unsigned int** err, int* num_sms);
 
 }  // namespace qat
