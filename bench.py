@@ -232,7 +232,7 @@ def run_ours(args, w):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sm = w.sm_scale
-    launches_per_step = 4  # fwd kernel; bwd preprocess, dK/dV kernel, dQ kernel
+    launches_per_step = 4  # fwd kernel; bwd prep, tcgen05 main, dQ convert kernels
 
     def fwd():
         st = capi.qat_attn_fwd(x["q"], x["k"], x["v"], o_q, o_hp, lse, B, H, Nq, Nkv, D, sm,
@@ -342,7 +342,7 @@ def run_ours(args, w):
         "tflops_flash_convention": world * 14.0 * pairs * D * args.steps / (total_ms * 1e-3) / 1e12,
         "tokens_per_s": world * B * Nq * args.steps / (total_ms * 1e-3),
         "roofline": {
-            "kernel": "qat_attn_bwd call (preprocess + dK/dV + dQ kernels)",
+            "kernel": "qat_attn_bwd call (prep + attn_bwd_tc_kernel + dQ convert)",
             "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
             "frac": bwd_tf / peak_sus, "traffic": None,
             "peak_kind": f"bf16_tflops_sustained ({peak_src})",

@@ -1,0 +1,578 @@
+// attn_bwd_sm100.cu -- QAT attention backward (straight-through estimator) on the
+// Blackwell tensor core (tcgen05 + TMEM + TMA), warp-specialized and persistent.
+//
+// Gradients of L = <dO, O_hp> ("attn_qat_train.py", _attn_bwd_preprocess,
+// _attn_bwd_dkdv, _attn_bwd_dq; P rematerialized from the saved base-2 lse as
+// "support for pytorch autograd" suggests):
+//   Delta_i = sum_d dO_id O_hp,id
+//   P^T = exp2(S^T qk_scale - lse)     S^T = K Q^T
+//   dP^T = V dO^T,   dS^T = P^T o (dP^T - Delta)
+//   dV += P^T dO,    dK += dS^T Q,    dQ += dS K     (dK, dQ scaled by sm_scale at the end)
+//
+// Kernels, in launch order on the caller's stream:
+//   bwd_prep_kernel     Delta and a copy of lse padded to 128-row blocks (+inf in the
+//                       padding, so P = 0 there), and zeroes the fp32 dQ accumulator.
+//   attn_bwd_tc_kernel  one CTA per SM, persistent over (head, 128-key block) items.
+//   dq_convert_kernel   dQ = bf16(dQ_acc * sm_scale).
+//
+// attn_bwd_tc_kernel, 320 threads:
+//   warp 0      TMA producer: K, V once per item; per 128-row query block Q (2-stage
+//               ring, with its lse and Delta rows by 1-D bulk copy) and dO (1 stage).
+//   warp 1      TMEM allocator; lane 0 issues all MMAs:
+//                 S^T  = K Q^T     SS  -> TMEM [0,128)      (A = K, B = Q, both K-major)
+//                 dP^T = V dO^T    SS  -> TMEM [128,256)
+//                 dV  += P^T dO    TS  (A = P^T in TMEM [0,64) bf16, B = dO MN-major)
+//                 dQ   = dS K      SS  -> TMEM [128,128+D)   (A = dS: the dS^T smem tile
+//                                       read MN-major; B = K MN-major)
+//                 dK  += dS^T Q    SS  (A = dS^T K-major, B = Q MN-major)
+//               steady-state order per block b: dV_b, S^T_{b+1}, dQ_b, dK_b, dP^T_{b+1},
+//               so the softmax warps and the dQ drain overlap tensor-core work.
+//   warps 2-5   softmax: one thread per key row (TMEM lane).  P phase: P^T from S^T,
+//               bf16 into TMEM for dV.  dS phase: dS^T from dP^T, bf16 into a 128-byte
+//               swizzled smem tile.  Epilogue of each item: dK, dV -> bf16 global.
+//   warps 6-9   dQ drain: one thread per query row; reads dQ_b from TMEM and adds it to
+//               the fp32 accumulator with vector atomics.
+// TMEM (512 columns): S^T [0,128), dP^T / dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
+#include "qat_internal.h"
+#include "sm100.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+namespace qat {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBlk = 128;       // keys per item, queries per block
+constexpr int kThreads = 320;
+
+template <int D>
+struct BwdTc {
+  static constexpr int kChunks = D / 64;
+  static constexpr uint32_t kChunkBytes = kBlk * 128;      // 16 KB box: 128 rows x 128 B
+  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffV = kOffK + kTileBytes;
+  static constexpr uint32_t kOffQ = kOffV + kTileBytes;     // 2 stages
+  static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;
+  static constexpr uint32_t kOffDS = kOffDO + kTileBytes;   // 128 x 128 bf16, 2 chunks
+  static constexpr uint32_t kOffLse = kOffDS + 2 * kChunkBytes;  // 2 stages x 512 B
+  static constexpr uint32_t kOffDelta = kOffLse + 1024;          // 2 stages x 512 B
+  static constexpr uint32_t kOffBar = kOffDelta + 1024;
+  static constexpr uint32_t kOffMisc = kOffBar + 256;
+  static constexpr uint32_t kUsed = kOffMisc + 64;
+  static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
+  static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDV = 256, kTmemDK = 256 + D;
+};
+
+enum : uint32_t {
+  B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL,
+  B_DO_EMPTY, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL, B_DS_EMPTY, B_DQ_FULL, B_DQ_EMPTY,
+  B_DKDV_FULL, B_DKDV_EMPTY, B_DRAIN, B_COUNT
+};
+
+struct BwdTcParams {
+  BwdArgs a;
+  unsigned int* err;
+  int mtiles;   // query blocks per head
+  int ktiles;   // key blocks per head
+  int items;    // B * H * ktiles
+  int nq_pad;   // mtiles * 128
+};
+
+__device__ __forceinline__ void bwd_item(int idx, const BwdTcParams& p, int& bh, int& kb,
+                                         int& first, int& count) {
+  const int BH = p.a.B * p.a.H;
+  if (p.a.causal) {  // longest first: small key blocks see the most queries
+    kb = idx / BH;
+    bh = idx % BH;
+    first = kb;
+    count = p.mtiles - kb;
+  } else {           // head-major; each item starts at a different query block so that
+    bh = idx / p.ktiles;  // the CTAs of one head spread their dQ atomics
+    kb = idx % p.ktiles;
+    first = kb % p.mtiles;
+    count = p.mtiles;
+  }
+}
+
+__device__ __forceinline__ int block_at(int first, int ii, const BwdTcParams& p) {
+  int b = first + ii;
+  if (!p.a.causal && b >= p.mtiles) b -= p.mtiles;
+  return b;
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmDO, const BwdTcParams p) {
+  using C = BwdTc<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 8);
+  const uint32_t bars = base + C::kOffBar;
+  auto bar = [&](uint32_t i) { return bars + 8u * i; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (uint32_t i = 0; i < B_COUNT; ++i) {
+      const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DQ_EMPTY ||
+                            i == B_DKDV_EMPTY) ? 128u : 1u;
+      mbar_init(bar(i), cnt);
+    }
+    fence_barrier_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t qc = 0, dc = 0;  // Q loads, dO loads issued
+      int it = 0;
+      bool ok = true;
+      auto load_q = [&](int bh, int blk) -> bool {
+        const uint32_t st = qc & 1, use = qc >> 1;
+        if (!mbar_wait(bar(B_Q_EMPTY0 + st), (use & 1) ^ 1, abort_flag, p.err)) return false;
+        const uint32_t fb = bar(B_Q_FULL0 + st);
+        mbar_arrive_expect_tx(fb, C::kTileBytes + 1024);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(base + C::kOffQ + st * C::kTileBytes + c * C::kChunkBytes, &tmQ, fb, 64 * c,
+                      blk * kBlk, bh);
+        const size_t row0 = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(blk) * kBlk;
+        bulk_load(base + C::kOffLse + st * 512, p.a.lse_pad + row0, 512, fb);
+        bulk_load(base + C::kOffDelta + st * 512, p.a.delta + row0, 512, fb);
+        ++qc;
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, kb, first, count;
+        bwd_item(idx, p, bh, kb, first, count);
+        ok = mbar_wait(bar(B_KV_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(base + C::kOffK + c * C::kChunkBytes, &tmK, bar(B_KV_FULL), 64 * c,
+                      kb * kBlk, bh);
+          tma_load_3d(base + C::kOffV + c * C::kChunkBytes, &tmV, bar(B_KV_FULL), 64 * c,
+                      kb * kBlk, bh);
+        }
+        ok = load_q(bh, block_at(first, 0, p));
+        for (int ii = 0; ii < count && ok; ++ii) {
+          const int blk = block_at(first, ii, p);
+          ok = mbar_wait(bar(B_DO_EMPTY), (dc & 1) ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(B_DO_FULL), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(base + C::kOffDO + c * C::kChunkBytes, &tmDO, bar(B_DO_FULL), 64 * c,
+                        blk * kBlk, bh);
+          ++dc;
+          if (ii + 1 < count) ok = load_q(bh, block_at(first, ii + 1, p));
+        }
+      }
+      // drain: every issued load lands before the CTA exits
+      if (it > 0) mbar_wait(bar(B_KV_FULL), (it - 1) & 1, abort_flag, p.err);
+      for (uint32_t i = (qc > 2 ? qc - 2 : 0); i < qc; ++i)
+        mbar_wait(bar(B_Q_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
+      if (dc > 0) mbar_wait(bar(B_DO_FULL), (dc - 1) & 1, abort_flag, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T, dP^T
+      constexpr uint32_t idKM = idesc_bf16_f32(kBlk, D, true, false);      // dV, dK
+      constexpr uint32_t idMM = idesc_bf16_f32(kBlk, D, true, true);       // dQ
+      const uint32_t sK = base + C::kOffK, sV = base + C::kOffV, sDO = base + C::kOffDO;
+      const uint32_t sDS = base + C::kOffDS;
+      uint32_t qc = 0;  // query blocks processed (global)
+      int it = 0;
+      bool ok = true, issued = false;
+      auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
+      auto issue_s = [&](uint32_t c) -> bool {  // S^T_c = K Q_c^T
+        const uint32_t st = c & 1;
+        if (!w(bar(B_Q_FULL0 + st), (c >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t sQ = base + C::kOffQ + st * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          mma_ss(tbase + C::kTmemS, smem_desc_sw128(sK + off, 16, 1024),
+                 smem_desc_sw128(sQ + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_S_FULL));
+        issued = true;
+        return true;
+      };
+      auto issue_dp = [&](uint32_t c) -> bool {  // dP^T_c = V dO_c^T (after dQ_{c-1} drained)
+        if (!w(bar(B_DO_FULL), c & 1)) return false;
+        if (c > 0 && !w(bar(B_DQ_EMPTY), (c - 1) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          mma_ss(tbase + C::kTmemDP, smem_desc_sw128(sV + off, 16, 1024),
+                 smem_desc_sw128(sDO + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_DP_FULL));
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, kb, first, count;
+        bwd_item(idx, p, bh, kb, first, count);
+        ok = w(bar(B_KV_FULL), it & 1) && issue_s(qc) && issue_dp(qc);
+        for (int ii = 0; ii < count && ok; ++ii, ++qc) {
+          const uint32_t st = qc & 1;
+          const uint32_t sQ = base + C::kOffQ + st * C::kTileBytes;
+          // dV += P^T dO
+          if (!(ok = w(bar(B_P_FULL), qc & 1))) break;
+          if (ii == 0 && !(ok = w(bar(B_DKDV_EMPTY), (it & 1) ^ 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kBlk / 16; ++ks)
+            mma_ts(tbase + C::kTmemDV, tbase + C::kTmemS + 8 * ks,
+                   smem_desc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idKM,
+                   (ii > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(B_DO_EMPTY));
+          if (ii + 1 < count && !(ok = issue_s(qc + 1))) break;
+          // dQ = dS K, then dK += dS^T Q
+          if (!(ok = w(bar(B_DS_FULL), qc & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kBlk / 16; ++ks)
+            mma_ss(tbase + C::kTmemDP, smem_desc_sw128(sDS + ks * 2048, C::kChunkBytes, 1024),
+                   smem_desc_sw128(sK + ks * 2048, C::kChunkBytes, 1024), idMM,
+                   ks > 0 ? 1u : 0u);
+          mma_commit(bar(B_DQ_FULL));
+#pragma unroll
+          for (int ks = 0; ks < kBlk / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+            mma_ss(tbase + C::kTmemDK, smem_desc_sw128(sDS + off, 16, 1024),
+                   smem_desc_sw128(sQ + ks * 2048, C::kChunkBytes, 1024), idKM,
+                   (ii > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(B_Q_EMPTY0 + st));
+          mma_commit(bar(B_DS_EMPTY));
+          if (ii + 1 < count && !(ok = issue_dp(qc + 1))) break;
+        }
+        if (!ok) break;
+        mma_commit(bar(B_KV_EMPTY));
+        mma_commit(bar(B_DKDV_FULL));
+      }
+      if (issued) {
+        mma_commit(bar(B_DRAIN));
+        mbar_wait(bar(B_DRAIN), 0, abort_flag, p.err);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ softmax (key rows)
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;               // key row within the block
+    const uint32_t lrow = (32u * quarter) << 16;
+    const float qk = p.a.qk_scale;
+    auto wwait = [&](uint32_t b_, uint32_t par) {
+      const bool okw = mbar_wait(b_, par, abort_flag, p.err);
+      return __all_sync(0xffffffffu, okw) != 0;
+    };
+    const uint32_t dsrow = base + C::kOffDS + r * 128;  // this row in dS^T chunk 0
+    const uint32_t sw = static_cast<uint32_t>(r & 7);
+    uint32_t qc = 0;
+    int it = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+      int bh, kb, first, count;
+      bwd_item(idx, p, bh, kb, first, count);
+      const int key = kb * kBlk + r;
+      const bool key_ok = key < p.a.Nkv;
+      for (int ii = 0; ii < count && ok; ++ii, ++qc) {
+        const int blk = block_at(first, ii, p);
+        const uint32_t st = qc & 1;
+        const float* sl = reinterpret_cast<const float*>(gbase + C::kOffLse + st * 512);
+        const float* sd = reinterpret_cast<const float*>(gbase + C::kOffDelta + st * 512);
+        // ---- P phase
+        ok = wwait(bar(B_Q_FULL0 + st), (qc >> 1) & 1) && wwait(bar(B_S_FULL), qc & 1);
+        if (!ok) break;
+        tc_fence_after();
+        const bool diag = p.a.causal && blk == kb;
+        const int q0 = blk * kBlk;
+        float P[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(tbase + lrow + C::kTmemS + 32 * c, sr);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(sl + 32 * c + i);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float pv = ex2f(fmaf(__uint_as_float(sr[i + e]), qk, -lv[e]));
+              if (!key_ok || (diag && q0 + 32 * c + i + e < key)) pv = 0.f;
+              P[32 * c + i + e] = pv;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(P[32 * c + 2 * i], P[32 * c + 2 * i + 1]);
+          tmem_st16(tbase + lrow + C::kTmemS + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(B_P_FULL));
+        // ---- dS phase
+        ok = wwait(bar(B_DP_FULL), qc & 1);
+        if (ok && qc > 0) ok = wwait(bar(B_DS_EMPTY), (qc - 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dr[32];
+          tmem_ld32(tbase + lrow + C::kTmemDP + 32 * c, dr);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(sd + 32 * c + i);
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float ds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              ds[e] = P[32 * c + i + e] * (__uint_as_float(dr[i + e]) - dv[e]);
+            pk[i / 2] = pack_bf16x2(ds[0], ds[1]);
+            pk[i / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          }
+          // queries [32c, 32c+32) = 16-byte units 4(c%2) .. 4(c%2)+3 of chunk c/2,
+          // each stored at its 128-byte-swizzled position (unit ^ row%8)
+          const uint32_t rowaddr = dsrow + (c >> 1) * C::kChunkBytes;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t unit = static_cast<uint32_t>(4 * (c & 1) + u) ^ sw;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowaddr + unit * 16),
+                         "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]),
+                         "r"(pk[4 * u + 3])
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(B_DS_FULL));
+      }
+      if (!ok) break;
+      // ---- epilogue: dV, dK rows of this item
+      ok = wwait(bar(B_DKDV_FULL), it & 1);
+      if (!ok) break;
+      tc_fence_after();
+      const size_t grow = (static_cast<size_t>(bh) * p.a.Nkv + (key_ok ? key : 0)) * D;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t tcol = half ? C::kTmemDK : C::kTmemDV;
+        uint16_t* out = half ? p.a.dk : p.a.dv;
+        const float scale = half ? p.a.sm_scale : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tbase + lrow + tcol + 32 * c, o);
+          tmem_wait_ld();
+          uint32_t wv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            wv[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * scale,
+                                __uint_as_float(o[2 * i + 1]) * scale);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + grow + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_DKDV_EMPTY));
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain (query rows)
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;
+    const uint32_t lrow = (32u * quarter) << 16;
+    auto wwait = [&](uint32_t b_, uint32_t par) {
+      const bool okw = mbar_wait(b_, par, abort_flag, p.err);
+      return __all_sync(0xffffffffu, okw) != 0;
+    };
+    uint32_t qc = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x) {
+      int bh, kb, first, count;
+      bwd_item(idx, p, bh, kb, first, count);
+      for (int ii = 0; ii < count; ++ii, ++qc) {
+        const int q = block_at(first, ii, p) * kBlk + r;
+        ok = wwait(bar(B_DQ_FULL), qc & 1);
+        if (!ok) break;
+        tc_fence_after();
+        float* acc = p.a.dq_acc + (static_cast<size_t>(bh) * p.a.Nq + (q < p.a.Nq ? q : 0)) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tbase + lrow + C::kTmemDP + 32 * c, o);
+          tmem_wait_ld();
+          if (q < p.a.Nq) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              atomicAdd(reinterpret_cast<float4*>(acc + 32 * c + 4 * v),
+                        make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                    __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_DQ_EMPTY));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ small kernels
+
+// One warp per padded query row: Delta, lse copy (+inf in padding), dQ accumulator = 0.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
+  constexpr int PER = D / 32;
+  const long long rows = static_cast<long long>(a.B) * a.H * nq_pad;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (long long rw = warp0; rw < rows; rw += nw) {
+    const long long bh = rw / nq_pad;
+    const int q = static_cast<int>(rw % nq_pad);
+    if (q >= a.Nq) {
+      if (lane == 0) {
+        a.delta[rw] = 0.f;
+        a.lse_pad[rw] = INFINITY;
+      }
+      continue;
+    }
+    const long long src = (bh * a.Nq + q) * D + lane * PER;
+    float acc = 0.f;
+    if constexpr (PER == 4) {
+      const uint2 ov = *reinterpret_cast<const uint2*>(a.o_hp + src);
+      const uint2 dv = *reinterpret_cast<const uint2*>(a.dO + src);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float2 of = __bfloat1622float2(o2[i]);
+        const float2 df = __bfloat1622float2(d2[i]);
+        acc = fmaf(of.x, df.x, acc);
+        acc = fmaf(of.y, df.y, acc);
+      }
+      *reinterpret_cast<float4*>(a.dq_acc + src) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const uint32_t ov = *reinterpret_cast<const uint32_t*>(a.o_hp + src);
+      const uint32_t dv = *reinterpret_cast<const uint32_t*>(a.dO + src);
+      const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
+      const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv));
+      acc = fmaf(of.x, df.x, of.y * df.y);
+      *reinterpret_cast<float2*>(a.dq_acc + src) = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      a.delta[rw] = acc;
+      a.lse_pad[rw] = a.lse[bh * a.Nq + q];
+    }
+  }
+}
+
+// dQ = bf16(dQ_acc * sm_scale), 8 elements per thread-step.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
+                                                         uint16_t* __restrict__ dq, float scale,
+                                                         long long n8) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += stride) {
+    const float4 x = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 y = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    reinterpret_cast<uint4*>(dq)[i] =
+        make_uint4(pack_bf16x2(x.x * scale, x.y * scale), pack_bf16x2(x.z * scale, x.w * scale),
+                   pack_bf16x2(y.x * scale, y.y * scale), pack_bf16x2(y.z * scale, y.w * scale));
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
+  using C = BwdTc<D>;
+  const int BH = a.B * a.H;
+  BwdTcParams p;
+  p.a = a;
+  p.err = err;
+  p.mtiles = (a.Nq + kBlk - 1) / kBlk;
+  p.ktiles = (a.Nkv + kBlk - 1) / kBlk;
+  p.items = BH * p.ktiles;
+  p.nq_pad = p.mtiles * kBlk;
+
+  const long long prow = static_cast<long long>(BH) * p.nq_pad;
+  long long pblocks = (prow + 7) / 8;
+  if (pblocks > static_cast<long long>(num_sms) * 64) pblocks = static_cast<long long>(num_sms) * 64;
+  bwd_prep_kernel<D><<<static_cast<unsigned>(pblocks), 256, 0, s>>>(a, p.nq_pad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bf16_map_3d(&mq, a.q, D, a.Nq, BH) || !make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) ||
+      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) || !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(C::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int grid = p.items < num_sms ? p.items : num_sms;
+  attn_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const long long n8 = static_cast<long long>(BH) * a.Nq * D / 8;
+  long long cblocks = (n8 + 255) / 256;
+  if (cblocks > static_cast<long long>(num_sms) * 32) cblocks = static_cast<long long>(num_sms) * 32;
+  dq_convert_kernel<<<static_cast<unsigned>(cblocks), 256, 0, s>>>(a.dq_acc, a.dq, a.sm_scale, n8);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
+  return a.D == 64 ? launch_bwd_tc_d<64>(a, err, num_sms, s)
+                   : launch_bwd_tc_d<128>(a, err, num_sms, s);
+}
+
+}  // namespace qat

@@ -427,42 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); boxes of 64 x 128 x 1.
-bool make_map(CUtensorMap* m, const void* ptr, int D, int N, int BH) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(N) * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_fwd_tc_d(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
   using C = FwdTc<D>;
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, D, a.Nq, BH) || !make_map(&mk, a.k, D, a.Nkv, BH) ||
-      !make_map(&mv, a.v, D, a.Nkv, BH))
+  if (!make_bf16_map_3d(&mq, a.q, D, a.Nq, BH) || !make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) ||
+      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH))
     return cudaErrorInvalidValue;
   TcParams p;
   p.a = a;
@@ -479,6 +450,38 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a, unsigned int* err, int num_sms, cu
 }
 
 }  // namespace
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(N) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
   return a.D == 64 ? launch_fwd_tc_d<64>(a, err, num_sms, s)

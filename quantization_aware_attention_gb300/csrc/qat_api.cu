@@ -137,8 +137,7 @@ qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v, void* o_q
 size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D) {
   bool empty = false;
   if (check_sizes(B, H, Nq, Nkv, D, 1.0f, 0, 0, &empty) != QAT_OK) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * Nq;
-  return round_up(rows * sizeof(float) > 0 ? rows * sizeof(float) : 1);
+  return qat::bwd_workspace_layout(B, H, Nq, D).total;
 }
 
 qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const void* o_hp,
@@ -167,6 +166,8 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return QAT_ERR_INVALID_ARG;
 
   qat::BwdArgs a;
+  const qat::BwdWorkspace wl = qat::bwd_workspace_layout(B, H, Nq, D);
+  char* ws = static_cast<char*>(workspace);
   a.q = static_cast<const uint16_t*>(q);
   a.k = static_cast<const uint16_t*>(k);
   a.v = static_cast<const uint16_t*>(v);
@@ -176,13 +177,17 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.dq = static_cast<uint16_t*>(dq);
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
-  a.delta = static_cast<float*>(workspace);
+  a.lse_pad = reinterpret_cast<float*>(ws + wl.off_lse);
+  a.delta = reinterpret_cast<float*>(ws + wl.off_delta);
+  a.dq_acc = reinterpret_cast<float*>(ws + wl.off_dq);
   a.B = B; a.H = H; a.Nq = Nq; a.Nkv = Nkv; a.D = D;
   a.sm_scale = sm_scale;
   a.qk_scale = sm_scale * kLog2e;
   a.causal = causal;
-  cudaError_t e = qat::launch_bwd_preprocess(a, s);
-  if (e == cudaSuccess) e = qat::launch_bwd_mma(a, s);
+  unsigned int* err = nullptr;
+  int num_sms = 0;
+  cudaError_t e = qat::device_context(&err, &num_sms);
+  if (e == cudaSuccess) e = qat::launch_bwd_tc(a, err, num_sms, s);
   return from_cuda(e);
 }
 

@@ -1,11 +1,35 @@
 // qat_internal.h -- declarations shared by the library's translation units (not ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace qat {
+
+// Backward workspace: [lse_pad | delta | dq_acc], each piece 256-byte aligned; query rows
+// are padded per head to a multiple of 128 for lse_pad and delta.
+struct BwdWorkspace {
+  size_t nq_pad, off_lse, off_delta, off_dq, total;
+};
+
+inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int D) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  BwdWorkspace w;
+  w.nq_pad = (static_cast<size_t>(Nq) + 127) / 128 * 128;
+  const size_t rows_pad = static_cast<size_t>(B) * H * w.nq_pad;
+  w.off_lse = 0;
+  w.off_delta = up(rows_pad * sizeof(float));
+  w.off_dq = w.off_delta + up(rows_pad * sizeof(float));
+  w.total = w.off_dq + up(static_cast<size_t>(B) * H * Nq * D * sizeof(float));
+  if (w.total == 0) w.total = 256;
+  return w;
+}
+
+// [BH, N, D] bf16 viewed as a 3-D TMA tensor (D innermost), 64 x 128 x 1 boxes,
+// 128-byte swizzle, zero fill out of bounds.
+bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH);
 
 // Arguments of one forward launch (device pointers, validated by the ABI layer).
 struct FwdArgs {
@@ -33,7 +57,9 @@ struct BwdArgs {
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
-  float* delta;     // fp32 [B, H, Nq] in the workspace
+  float* delta;     // fp32 [B, H, Nq_pad] in the workspace (0 in padding rows)
+  float* lse_pad;   // fp32 [B, H, Nq_pad] copy of lse (+inf in padding rows)
+  float* dq_acc;    // fp32 [B, H, Nq, D] dQ accumulator in the workspace
   int B, H, Nq, Nkv, D;
   float sm_scale;
   float qk_scale;
@@ -42,8 +68,7 @@ struct BwdArgs {
 
 // Kernel launchers (return cudaGetLastError() after the launches).
 cudaError_t launch_fwd_tc(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
-cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
-cudaError_t launch_bwd_mma(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_tc(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
 cudaError_t launch_debug_quant(const float* p, int rows, int cols, float* deq,
                                float* scales, uint8_t* codes, cudaStream_t s);
 

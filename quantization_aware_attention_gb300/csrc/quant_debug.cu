@@ -2,7 +2,6 @@
 // to caller-supplied fp32 tiles so the rule can be compared bit for bit with the
 // specification (one warp per row x 64-column tile, two columns per lane).
 #include "qat_internal.h"
-#include "qat_mma.cuh"
 #include "qat_quant.cuh"
 
 namespace qat {
