@@ -217,7 +217,11 @@ def run_ours(args, w):
     capi.lib()
 
     B, H, Nq, Nkv, D = w.B, w.H, w.Nq, w.Nkv, w.D
-    inp = make_inputs(w)
+    if w.name == "custom":
+        from quantization_aware_attention_gb300.inputs import custom_inputs
+        inp = custom_inputs(9000, B, H, Nq, Nkv, D)
+    else:
+        inp = make_inputs(w)
     host = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
             for n, a in inp.items()}
     del inp
@@ -236,14 +240,14 @@ def run_ours(args, w):
 
     def fwd():
         st = capi.qat_attn_fwd(x["q"], x["k"], x["v"], o_q, o_hp, lse, B, H, Nq, Nkv, D, sm,
-                               0, capi.QUANT_P_FP8E4M3_ROW_TILE64, stream)
+                               int(w.causal), capi.QUANT_P_FP8E4M3_ROW_TILE64, stream)
         if st != capi.Status.OK:
             raise capi.QatError(st, "qat_attn_fwd")
 
     def bwd():
         st = capi.qat_attn_bwd(x["q"], x["k"], x["v"], o_hp, lse, x["do"], dq, dk, dv, B, H, Nq,
-                               Nkv, D, sm, 0, capi.QUANT_P_FP8E4M3_ROW_TILE64, ws, ws_bytes,
-                               stream)
+                               Nkv, D, sm, int(w.causal), capi.QUANT_P_FP8E4M3_ROW_TILE64, ws,
+                               ws_bytes, stream)
         if st != capi.Status.OK:
             raise capi.QatError(st, "qat_attn_bwd")
 
@@ -292,10 +296,12 @@ def run_ours(args, w):
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
     # ---- end to end: host buffers, copies inside the timed region
-    hout = {n: torch.empty(host["q"].shape, dtype=torch.bfloat16).pin_memory()
-            for n in ("o_q", "dq")}
-    hout.update({n: torch.empty(host["k"].shape, dtype=torch.bfloat16).pin_memory()
-                 for n in ("dk", "dv")})
+    hout = {}
+    if not args.no_e2e:
+        hout = {n: torch.empty(host["q"].shape, dtype=torch.bfloat16).pin_memory()
+                for n in ("o_q", "dq")}
+        hout.update({n: torch.empty(host["k"].shape, dtype=torch.bfloat16).pin_memory()
+                     for n in ("dk", "dv")})
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in hout.values())
     e2e_steps = max(1, min(args.steps, 5))
@@ -310,7 +316,10 @@ def run_ours(args, w):
         hout["dk"].copy_(dk, non_blocking=True)
         hout["dv"].copy_(dv, non_blocking=True)
 
-    e2e_step()
+    if args.no_e2e:
+        e2e_steps = 0
+    else:
+        e2e_step()
     barrier()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
@@ -320,7 +329,7 @@ def run_ours(args, w):
     s1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(s0.elapsed_time(s1))
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = (world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12) if e2e_steps else None
 
     # ---- roofline of the dominant kernel work (the backward call)
     peaks, peak_src = load_peaks()
@@ -379,11 +388,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,Nq,Nkv,D[,causal]: a smaller case for profiling instead of the "
+                         "benchmarked workload")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    from quantization_aware_attention_gb300.inputs import WORKLOADS
+    from quantization_aware_attention_gb300.inputs import WORKLOADS, Workload
     w = WORKLOADS[WORKLOAD]
+    if args.shape:
+        v = [int(x) for x in args.shape.split(",")]
+        w = Workload("custom", 9, v[0], v[1], v[2], v[3], v[4], causal=bool(v[5]) if len(v) > 5 else False)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

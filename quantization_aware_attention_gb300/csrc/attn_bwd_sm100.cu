@@ -323,27 +323,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool diag = p.a.causal && blk == kb;
         const int q0 = blk * kBlk;
-        float P[128];
+        // P^T kept as bf16 pairs between the two phases (the values dV consumes); the
+        // register file allows 168 registers per thread with 10 warps per CTA
+        uint32_t Pp[64];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t sr[32];
           tmem_ld32(tbase + lrow + C::kTmemS + 32 * c, sr);
           tmem_wait_ld();
-          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(sl + 32 * c + i);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float pv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float pv = ex2f(fmaf(__uint_as_float(sr[i + e]), qk, -lv[e]));
-              if (!key_ok || (diag && q0 + 32 * c + i + e < key)) pv = 0.f;
-              P[32 * c + i + e] = pv;
+              pv[e] = ex2f(fmaf(__uint_as_float(sr[i + e]), qk, -lv[e]));
+              if (!key_ok || (diag && q0 + 32 * c + i + e < key)) pv[e] = 0.f;
             }
+            Pp[16 * c + i / 2] = pack_bf16x2(pv[0], pv[1]);
+            Pp[16 * c + i / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
           }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(P[32 * c + 2 * i], P[32 * c + 2 * i + 1]);
-          tmem_st16(tbase + lrow + C::kTmemS + 16 * c, pk);
+          tmem_st16(tbase + lrow + C::kTmemS + 16 * c,
+                    *reinterpret_cast<const uint32_t(*)[16]>(&Pp[16 * c]));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -364,9 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 d4 = *reinterpret_cast<const float4*>(sd + 32 * c + i);
             const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
             float ds[4];
+            const uint32_t pa = Pp[16 * c + i / 2], pb = Pp[16 * c + i / 2 + 1];
+            const float pvv[4] = {__uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u),
+                                  __uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              ds[e] = P[32 * c + i + e] * (__uint_as_float(dr[i + e]) - dv[e]);
+              ds[e] = pvv[e] * (__uint_as_float(dr[i + e]) - dv[e]);
             pk[i / 2] = pack_bf16x2(ds[0], ds[1]);
             pk[i / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
           }

@@ -7,7 +7,7 @@
 //   amax = max p, Pq = quant(p) (qat_quant.cuh);  O_q = alpha O_q + Pq V_j;
 //   O_hp = alpha O_hp + P V_j;  epilogue O / l, lse = m + log2 l.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over (head, 128-row q tile)):
+// CTA layout (320 threads, one CTA per SM, persistent over (head, 128-row q tile)):
 //   warp 0      TMA producer: Q tile once per work item, K tiles (3-stage ring) and
 //               V tiles (2-stage ring), 128 keys x D, 128-byte swizzled boxes.
 //   warp 1      TMEM allocator; lane 0 issues every tcgen05.mma:
@@ -16,9 +16,12 @@
 //                 O_hp += P_j V_j          (TS, same V descriptors: the two P tiles share V)
 //               issue order S_j, PV_{j-1}, S_{j+1}, ... so the tensor core computes the
 //               next scores while the softmax warps work on the current tile.
-//   warps 2-5   softmax + quantization, one thread per query row (TMEM lane), then the
-//               epilogue.  P is written back into the S buffer it came from as two bf16
-//               tiles (Pq in columns 0-63, P in 64-127), consumed by the TS MMAs.
+//   warps 2-9   softmax + quantization in two warpgroups: warps 2-5 take keys 0-63 and
+//               warps 6-9 keys 64-127 of each S row (one 64-key quantization tile per
+//               thread), exchanging the row max through shared memory.  P is written
+//               back into the S buffer it came from as two bf16 tiles (Pq in columns
+//               0-63, P in 64-127), consumed by the TS MMAs.  Epilogue: warps 2-5 store
+//               O_q and lse, warps 6-9 O_hp.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O_q [256,256+D), O_hp [256+D,256+2D).
 //
 // The running max is updated only when it grows by more than 8 (base-2 units), so P
@@ -44,7 +47,7 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 
 template <int D>
@@ -57,7 +60,8 @@ struct FwdTc {
   static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr uint32_t kOffMisc = kOffBar + 256;
-  static constexpr uint32_t kUsed = kOffMisc + 64;
+  static constexpr uint32_t kOffX = kOffMisc + 64;     // row-max / row-sum exchange, 3 KB
+  static constexpr uint32_t kUsed = kOffX + 3072;
   // at least 116 KB so that no two CTAs share an SM (each holds all 512 TMEM columns)
   static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
   static constexpr uint32_t kTmemOq = 256;
@@ -68,7 +72,7 @@ struct FwdTc {
 enum : uint32_t {
   BAR_Q_FULL = 0, BAR_Q_EMPTY = 1, BAR_K_FULL = 2, BAR_K_EMPTY = 5, BAR_V_FULL = 8,
   BAR_V_EMPTY = 10, BAR_S_FULL = 12, BAR_P_FULL = 14, BAR_O_DONE = 16, BAR_O_EMPTY = 17,
-  BAR_DRAIN = 18, BAR_COUNT = 19
+  BAR_DRAIN = 18, BAR_X = 19, BAR_COUNT = 20
 };
 
 struct TcParams {
@@ -141,11 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(BAR_S_FULL + b), 1);
-      mbar_init(bar(BAR_P_FULL + b), 128);
+      mbar_init(bar(BAR_P_FULL + b), 256);
     }
     mbar_init(bar(BAR_O_DONE), 1);
-    mbar_init(bar(BAR_O_EMPTY), 128);
+    mbar_init(bar(BAR_O_EMPTY), 256);
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_X), 256);
     fence_barrier_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
@@ -277,14 +282,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    // Two warpgroups: h = 0 (warps 2-5) owns keys 0-63 of every S row, h = 1 (warps
+    // 6-9) keys 64-127 -- each thread one row of one 64-key quantization tile.
+    const int h = (warp - 2) >> 2;
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int r = 32 * quarter + lane;            // row of the 128-row tile
     const uint32_t lrow = (32u * quarter) << 16;  // TMEM lane offset
     const float qk = p.a.qk_scale;
+    float* xmax = reinterpret_cast<float*>(gbase + C::kOffX);        // [2 parity][2 h][128]
+    float* xsum = reinterpret_cast<float*>(gbase + C::kOffX + 2048); // [2 h][128]
     // tcgen05.ld/st are warp-collective: every wait result is made warp-uniform
     auto wwait = [&](uint32_t b_, uint32_t par) {
       const bool w = mbar_wait(b_, par, abort_flag, p.err);
       return __all_sync(0xffffffffu, w) != 0;
+    };
+    // exchange between the two groups: every softmax thread arrives on BAR_X after
+    // writing its value and waits (bounded) for the phase before reading the other's
+    uint32_t xc = 0;
+    auto exchange = [&]() {
+      tc_fence_before();
+      mbar_arrive(bar(BAR_X));
+      const bool w = wwait(bar(BAR_X), xc & 1);
+      ++xc;
+      tc_fence_after();
+      return w;
     };
     uint32_t sc = 0, pvc = 0;                     // S tiles consumed, PV groups done
     int it = 0;
@@ -300,30 +321,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wwait(bar(BAR_S_FULL + b), (sc >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[128];
+        uint32_t sr[64];
         const uint32_t tS = tbase + lrow + b * 128;
-        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
         float* s = reinterpret_cast<float*>(sr);
-        const int key0 = j * kBN;
-        if (key0 + kBN > p.a.Nkv || (p.a.causal && j == mt)) {
+        const int key0 = j * kBN + 64 * h;
+        if (j * kBN + kBN > p.a.Nkv || (p.a.causal && j == mt)) {
           const int lim = p.a.causal ? min(p.a.Nkv - 1, row) : p.a.Nkv - 1;
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
+          for (int i = 0; i < 64; ++i)
             if (key0 + i > lim) s[i] = -INFINITY;
         }
-        float t0 = fmax3(s[0], s[1], s[2]), t1 = fmax3(s[64], s[65], s[66]);
+        float t = fmax3(s[0], s[1], s[2]);
 #pragma unroll
-        for (int i = 3; i < 63; i += 2) {
-          t0 = fmax3(t0, s[i], s[i + 1]);
-          t1 = fmax3(t1, s[64 + i], s[64 + i + 1]);
-        }
-        t0 = fmaxf(t0, s[63]);
-        t1 = fmaxf(t1, s[127]);
-        const float tmax = fmaxf(t0, t1) * qk;
+        for (int i = 3; i < 63; i += 2) t = fmax3(t, s[i], s[i + 1]);
+        t = fmaxf(t, s[63]);
+        // exchange the tile maxima of the row; the barrier also orders both groups'
+        // TMEM reads of S before either writes P over it
+        xmax[(j & 1) * 256 + h * 128 + r] = t;
+        if (!(ok = exchange())) break;
+        const float t_other = xmax[(j & 1) * 256 + (h ^ 1) * 128 + r];
+        const float tmax = fmaxf(t, t_other) * qk;
         float alpha = 1.f;
         bool resc = false;
         if (tmax > m_used + kRescaleThreshold) {
@@ -334,18 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = tmax;
         }
         const float negm = -m_used;
-        const TileScale ts0 = tile_scale(ex2(fmaf(t0, qk, negm)));
-        const TileScale ts1 = tile_scale(ex2(fmaf(t1, qk, negm)));
+        const TileScale ts = tile_scale(ex2(fmaf(t, qk, negm)));
         l *= alpha;
+        float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t pq[16], ph[16];
-          const TileScale ts = c < 2 ? ts0 : ts1;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(s[32 * c + 2 * i], qk, negm));
-            const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], qk, negm));
-            l += p0 + p1;
+            const float2 x = fma_rn_f32x2(make_float2(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]),
+                                          make_float2(qk, qk), make_float2(negm, negm));
+            const float p0 = ex2(x.x), p1 = ex2(x.y);
+            lsum = add_rn_f32x2(lsum, make_float2(p0, p1));
             ph[i] = pack_bf16(p0, p1);
             if (p.a.quant) {
               uint16_t cd;
@@ -355,27 +375,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               pq[i] = ph[i];
             }
           }
-          tmem_st16(tS + 16 * c, pq);
-          tmem_st16(tS + 64 + 16 * c, ph);
+          tmem_st16(tS + 32 * h + 16 * c, pq);
+          tmem_st16(tS + 64 + 32 * h + 16 * c, ph);
         }
+        l += lsum.x + lsum.y;
         tmem_wait_st();
         if (__any_sync(0xffffffffu, resc)) {
-          // O must hold every PV issued so far before it is rescaled
+          // O must hold every PV issued so far before it is rescaled; group h rescales
+          // O_q (h = 0) or O_hp (h = 1)
           ok = wwait(bar(BAR_O_DONE), (pvc - 1) & 1);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t tO = tbase + lrow + (h ? C::kTmemOhp : C::kTmemOq);
 #pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t tO = tbase + lrow + (half ? C::kTmemOhp : C::kTmemOq);
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tO + 32 * c, o);
-              tmem_wait_ld();
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tO + 32 * c, o);
-            }
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + 32 * c, o);
           }
           tmem_wait_st();
         }
@@ -386,39 +405,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
+      xsum[h * 128 + r] = l;
+      if (!(ok = exchange())) break;
+      const float l_row = xsum[r] + xsum[128 + r];
       ok = wwait(bar(BAR_O_DONE), (pvc - 1) & 1);
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = 1.0f / l_row;
       const bool in = row < p.a.Nq;
       const size_t orow = (static_cast<size_t>(bh) * p.a.Nq + (in ? row : 0)) * D;
+      const uint32_t tO = tbase + lrow + (h ? C::kTmemOhp : C::kTmemOq);
+      uint16_t* out = h ? p.a.o_hp : p.a.o_q;
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t tO = tbase + lrow + (half ? C::kTmemOhp : C::kTmemOq);
-        uint16_t* out = half ? p.a.o_hp : p.a.o_q;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
-          uint32_t w[16];
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (in) {
-            uint4* dst = reinterpret_cast<uint4*>(out + orow + 32 * c);
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (in) {
+          uint4* dst = reinterpret_cast<uint4*>(out + orow + 32 * c);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
       }
+      // (xsum is rewritten only after the next item's first exchange, which both
+      // groups reach after this read)
       tc_fence_before();
       mbar_arrive(bar(BAR_O_EMPTY));
-      if (in) p.a.lse[static_cast<size_t>(bh) * p.a.Nq + row] = m_used + log2f(l);
+      if (in && h == 0) p.a.lse[static_cast<size_t>(bh) * p.a.Nq + row] = m_used + log2f(l_row);
     }
   }
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -88,7 +90,16 @@ qat_status_t check_sizes(int B, int H, int Nq, int Nkv, int D, float sm_scale, i
   return QAT_OK;
 }
 
-qat_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QAT_OK : QAT_ERR_CUDA; }
+// With QAT_VERBOSE=1 in the environment, CUDA errors are also printed to stderr.
+qat_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return QAT_OK;
+  static const bool verbose = [] {
+    const char* v = getenv("QAT_VERBOSE");
+    return v != nullptr && v[0] == '1';
+  }();
+  if (verbose) fprintf(stderr, "qat_attn: CUDA error %d: %s\n", static_cast<int>(e), cudaGetErrorString(e));
+  return QAT_ERR_CUDA;
+}
 
 }  // namespace
 

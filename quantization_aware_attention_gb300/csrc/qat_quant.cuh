@@ -54,14 +54,48 @@ __device__ __forceinline__ float2 e4m3x2_decode(uint16_t codes) {
   return __half22float2(h);
 }
 
+// Packed fp32 pair helpers (two IEEE round-to-nearest operations per instruction).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 f2_unpack(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+__device__ __forceinline__ float2 mul_rn_f32x2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a.x, a.y)), "l"(f2_pack(b.x, b.y)));
+  return f2_unpack(d);
+}
+
+__device__ __forceinline__ float2 fma_rn_f32x2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(f2_pack(a.x, a.y)), "l"(f2_pack(b.x, b.y)), "l"(f2_pack(c.x, c.y)));
+  return f2_unpack(d);
+}
+
+__device__ __forceinline__ float2 add_rn_f32x2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a.x, a.y)), "l"(f2_pack(b.x, b.y)));
+  return f2_unpack(d);
+}
+
 // Quantize a pair of probabilities of one tile: returns the bf16 pair of quantized
-// values (lo in the low half), and the two code bytes through `codes`.
+// values (p0 in the low half), and the two code bytes through `codes`.
 __device__ __forceinline__ __nv_bfloat162 quant_pair(float p0, float p1, TileScale t,
                                                      uint16_t* codes) {
-  const uint16_t c = e4m3x2_rn_satfinite(__fmul_rn(p0, t.inv), __fmul_rn(p1, t.inv));
+  const float2 x = mul_rn_f32x2(make_float2(p0, p1), make_float2(t.inv, t.inv));
+  const uint16_t c = e4m3x2_rn_satfinite(x.x, x.y);
   *codes = c;
-  const float2 d = e4m3x2_decode(c);
-  return __floats2bfloat162_rn(__fmul_rn(d.x, t.scale), __fmul_rn(d.y, t.scale));
+  const float2 d = mul_rn_f32x2(e4m3x2_decode(c), make_float2(t.scale, t.scale));
+  return __floats2bfloat162_rn(d.x, d.y);
 }
 
 }  // namespace qat
