@@ -30,8 +30,8 @@
 //   warps 2-5   softmax: one thread per key row (TMEM lane).  P phase: P^T from S^T,
 //               bf16 into TMEM for dV.  dS phase: dS^T from dP^T, bf16 into a 128-byte
 //               swizzled smem tile.  Epilogue of each item: dK, dV -> bf16 global.
-//   warps 6-9   dQ drain: one thread per query row; reads dQ_b from TMEM and adds it to
-//               the fp32 accumulator with vector atomics.
+//   warps 6-9   dQ drain: one thread per query row; reads dQ_b from TMEM, frees the
+//               columns, and adds it to the fp32 accumulator by TMA bulk reduce-add.
 // TMEM (512 columns): S^T [0,128), dP^T / dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
 #include "qat_internal.h"
 #include "sm100.cuh"
@@ -58,7 +58,8 @@ struct BwdTc {
   static constexpr uint32_t kOffQ = kOffV + kTileBytes;     // 2 stages
   static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;
   static constexpr uint32_t kOffDS = kOffDO + kTileBytes;   // 128 x 128 bf16, 2 chunks
-  static constexpr uint32_t kOffLse = kOffDS + 2 * kChunkBytes;  // 2 stages x 512 B
+  static constexpr uint32_t kOffStage = kOffDS + 2 * kChunkBytes;  // dQ staging, 4 x 4 KB
+  static constexpr uint32_t kOffLse = kOffStage + 16384;         // 2 stages x 512 B
   static constexpr uint32_t kOffDelta = kOffLse + 1024;          // 2 stages x 512 B
   static constexpr uint32_t kOffBar = kOffDelta + 1024;
   static constexpr uint32_t kOffMisc = kOffBar + 256;
@@ -120,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmDO, const BwdTcParams p) {
+                       const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdTcParams p) {
   using C = BwdTc<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    prefetch_tmap(&tmDQ);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
@@ -425,9 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ drain (query rows)
+    // Reads the whole dQ_b row from TMEM (one thread per query row), releases the TMEM
+    // columns at once, then adds the rows to the fp32 accumulator 32 columns at a time
+    // through a 128-byte-swizzled 4 KB staging box and a TMA bulk reduce-add (full
+    // 128-byte lines; rows beyond Nq are clipped by the tensor bounds).
     const int quarter = warp & 3;
-    const int r = 32 * quarter + lane;
     const uint32_t lrow = (32u * quarter) << 16;
+    const uint32_t stage = base + C::kOffStage + quarter * 4096;
+    const uint32_t srow = stage + lane * 128;
+    const uint32_t sw = static_cast<uint32_t>(lane & 7);
     auto wwait = [&](uint32_t b_, uint32_t par) {
       const bool okw = mbar_wait(b_, par, abort_flag, p.err);
       return __all_sync(0xffffffffu, okw) != 0;
@@ -438,30 +447,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       int bh, kb, first, count;
       bwd_item(idx, p, bh, kb, first, count);
       for (int ii = 0; ii < count; ++ii, ++qc) {
-        const int q = block_at(first, ii, p) * kBlk + r;
+        const int q0 = block_at(first, ii, p) * kBlk;
         ok = wwait(bar(B_DQ_FULL), qc & 1);
         if (!ok) break;
         tc_fence_after();
-        float* acc = p.a.dq_acc + (static_cast<size_t>(bh) * p.a.Nq + (q < p.a.Nq ? q : 0)) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tbase + lrow + C::kTmemDP + 32 * c, o);
-          tmem_wait_ld();
-          if (q < p.a.Nq) {
+        uint32_t o[D];
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              atomicAdd(reinterpret_cast<float4*>(acc + 32 * c + 4 * v),
-                        make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                    __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
-          }
-        }
+        for (int c = 0; c < D / 32; ++c)
+          tmem_ld32(tbase + lrow + C::kTmemDP + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * c]));
+        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(B_DQ_EMPTY));
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          if (lane == 0) bulk_wait_read_all();  // the previous box has left the staging area
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + ((u ^ sw) * 16)),
+                         "r"(o[32 * c + 4 * u]), "r"(o[32 * c + 4 * u + 1]),
+                         "r"(o[32 * c + 4 * u + 2]), "r"(o[32 * c + 4 * u + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && q0 + 32 * quarter < p.a.Nq) {  // boxes past Nq hold no rows
+            tma_reduce_add_3d(&tmDQ, stage, 32 * c, q0 + 32 * quarter, bh);
+            bulk_commit_group();
+          }
+        }
       }
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -554,15 +572,16 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_bf16_map_3d(&mq, a.q, D, a.Nq, BH) || !make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) ||
-      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) || !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH))
+      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) || !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH) ||
+      !make_f32_map_3d(&mdq, a.dq_acc, D, a.Nq, BH))
     return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = p.items < num_sms ? p.items : num_sms;
-  attn_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, p);
+  attn_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, mdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
