@@ -21,17 +21,17 @@
 //   warp 1      TMEM allocator; lane 0 issues all MMAs:
 //                 S^T  = K Q^T     SS  -> TMEM [0,128)      (A = K, B = Q, both K-major)
 //                 dP^T = V dO^T    SS  -> TMEM [128,256)
-//                 dV  += P^T dO    TS  (A = P^T in TMEM [0,64) bf16, B = dO MN-major)
+//                 dV  += P^T dO    TS  (A = P^T bf16 in TMEM [0,32) + [64,96), B = dO MN-major)
 //                 dQ   = dS K      SS  -> TMEM [128,128+D)   (A = dS: the dS^T smem tile
 //                                       read MN-major; B = K MN-major)
 //                 dK  += dS^T Q    SS  (A = dS^T K-major, B = Q MN-major)
 //               steady-state order per block b: dV_b, S^T_{b+1}, dQ_b, dK_b, dP^T_{b+1},
 //               so the softmax warps and the dQ drain overlap tensor-core work.
-//   warps 2-5   softmax: one thread per key row (TMEM lane).  P phase: P^T from S^T,
-//               bf16 into TMEM for dV.  dS phase: dS^T from dP^T, bf16 into a 128-byte
-//               swizzled smem tile.  Epilogue of each item: dK, dV -> bf16 global.
-//   warps 6-9   dQ drain: one thread per query row; reads dQ_b from TMEM, frees the
-//               columns, and adds it to the fp32 accumulator by TMA bulk reduce-add.
+//   warps 2-9   two compute warpgroups, each owning 64 of a block's 128 query columns:
+//               P phase (P^T from S^T, bf16 into TMEM for dV), dS phase (dS^T from dP^T,
+//               bf16 into a 128-byte-swizzled smem tile), dQ drain (half of dQ's
+//               columns out of TMEM, then TMA bulk reduce-add into the fp32
+//               accumulator), and per item one of dV / dK -> bf16 global.
 // TMEM (512 columns): S^T [0,128), dP^T / dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
 #include "qat_internal.h"
 #include "sm100.cuh"
@@ -58,7 +58,7 @@ struct BwdTc {
   static constexpr uint32_t kOffQ = kOffV + kTileBytes;     // 2 stages
   static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;
   static constexpr uint32_t kOffDS = kOffDO + kTileBytes;   // 128 x 128 bf16, 2 chunks
-  static constexpr uint32_t kOffStage = kOffDS + 2 * kChunkBytes;  // dQ staging, 4 x 4 KB
+  static constexpr uint32_t kOffStage = kOffDS + 2 * kChunkBytes;  // dQ staging, 8 x 2 KB
   static constexpr uint32_t kOffLse = kOffStage + 16384;         // 2 stages x 512 B
   static constexpr uint32_t kOffDelta = kOffLse + 1024;          // 2 stages x 512 B
   static constexpr uint32_t kOffBar = kOffDelta + 1024;
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (uint32_t i = 0; i < B_COUNT; ++i) {
       const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DQ_EMPTY ||
-                            i == B_DKDV_EMPTY) ? 128u : 1u;
+                            i == B_DKDV_EMPTY) ? 256u : 1u;
       mbar_init(bar(i), cnt);
     }
     fence_barrier_init();
@@ -260,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ii == 0 && !(ok = w(bar(B_DKDV_EMPTY), (it & 1) ^ 1))) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks)
-            mma_ts(tbase + C::kTmemDV, tbase + C::kTmemS + 8 * ks,
+          for (int ks = 0; ks < kBlk / 16; ++ks)  // P^T halves at columns [0,32), [64,96)
+            mma_ts(tbase + C::kTmemDV, tbase + C::kTmemS + (ks < 4 ? 8 * ks : 32 + 8 * ks),
                    smem_desc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idKM,
                    (ii > 0 || ks > 0) ? 1u : 0u);
           mma_commit(bar(B_DO_EMPTY));
@@ -295,18 +295,142 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(B_DRAIN), 0, abort_flag, p.err);
       }
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ softmax (key rows)
+  } else {
+    // ------------------------------------------------------------ compute warpgroups
+    // Two warpgroups, h = 0 (warps 2-5) and h = 1 (warps 6-9); each thread owns one key
+    // row (TMEM lane) and query columns [64h, 64h + 64) of every block:
+    //   P phase   P^T = exp2(S^T qk_scale - lse) -> bf16 into TMEM columns [64h, 64h+32)
+    //   dS phase  dS^T = P^T o (dP^T - Delta) -> bf16 into chunk h of the dS^T smem tile
+    //   drain     dQ_b columns [hD/2, (h+1)D/2) (one thread per query row) -> TMA
+    //             reduce-add through a 64-byte-swizzled 2 KB staging box per warp
+    //   epilogue  h = 0 stores dV, h = 1 stores dK (x sm_scale) for the item's key rows.
+    const int h = (warp - 2) >> 2;
     const int quarter = warp & 3;
-    const int r = 32 * quarter + lane;               // key row within the block
+    const int r = 32 * quarter + lane;               // key row (and query row in the drain)
     const uint32_t lrow = (32u * quarter) << 16;
     const float qk = p.a.qk_scale;
     auto wwait = [&](uint32_t b_, uint32_t par) {
       const bool okw = mbar_wait(b_, par, abort_flag, p.err);
       return __all_sync(0xffffffffu, okw) != 0;
     };
-    const uint32_t dsrow = base + C::kOffDS + r * 128;  // this row in dS^T chunk 0
+    const uint32_t dsrow = base + C::kOffDS + h * C::kChunkBytes + r * 128;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
+    const uint32_t stage = base + C::kOffStage + (warp - 2) * 2048;
+    const uint32_t strow = stage + lane * 64;
+    const uint32_t sw64 = static_cast<uint32_t>((lane >> 1) & 3);
+    constexpr int kDrainCols = D / 2;
+    uint32_t Pp[32];                                  // P^T of the current block, bf16 pairs
+    // P phase of block `blk` (global index c): P^T -> TMEM for the dV MMA
+    auto p_phase = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
+      const uint32_t st = c & 1;
+      const float* sl = reinterpret_cast<const float*>(gbase + C::kOffLse + st * 512) + 64 * h;
+      if (!(wwait(bar(B_Q_FULL0 + st), (c >> 1) & 1) && wwait(bar(B_S_FULL), c & 1))) return false;
+      tc_fence_after();
+      const bool diag = p.a.causal && blk == kb;
+      const int qh = blk * kBlk + 64 * h;             // first query of this thread's columns
+      {
+        uint32_t sr[64];
+        tmem_ld32(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tbase + lrow + C::kTmemS + 64 * h + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pv[e] = ex2f(fmaf(__uint_as_float(sr[i + e]), qk, -lv[e]));
+            if (!key_ok || (diag && qh + i + e < key)) pv[e] = 0.f;
+          }
+          Pp[i / 2] = pack_bf16x2(pv[0], pv[1]);
+          Pp[i / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+        }
+      }
+      tmem_st16(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<const uint32_t(*)[16]>(&Pp[0]));
+      tmem_st16(tbase + lrow + C::kTmemS + 64 * h + 16,
+                *reinterpret_cast<const uint32_t(*)[16]>(&Pp[16]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_FULL));
+      return true;
+    };
+    // dS phase of block c: dS^T = P^T o (dP^T - Delta) -> bf16 into the dS^T smem tile
+    auto ds_phase = [&](uint32_t c) -> bool {
+      const float* sd =
+          reinterpret_cast<const float*>(gbase + C::kOffDelta + (c & 1) * 512) + 64 * h;
+      bool okd = wwait(bar(B_DP_FULL), c & 1);
+      if (okd && c > 0) okd = wwait(bar(B_DS_EMPTY), (c - 1) & 1);
+      if (!okd) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t dr[32];
+        tmem_ld32(tbase + lrow + C::kTmemDP + 64 * h + 32 * cc, dr);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(sd + 32 * cc + i);
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          const uint32_t pa = Pp[16 * cc + i / 2], pb = Pp[16 * cc + i / 2 + 1];
+          const float pvv[4] = {__uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u),
+                                __uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)};
+          float ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ds[e] = pvv[e] * (__uint_as_float(dr[i + e]) - dv[e]);
+          pk[i / 2] = pack_bf16x2(ds[0], ds[1]);
+          pk[i / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        // queries [32cc, 32cc + 32) of chunk h are 16-byte units 4cc .. 4cc + 3 of this
+        // row, each at its 128-byte-swizzled position (unit ^ row % 8)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t unit = static_cast<uint32_t>(4 * cc + u) ^ sw;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dsrow + unit * 16),
+                       "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_DS_FULL));
+      return true;
+    };
+    // drain of block c: this group's dQ columns out of TMEM (TMEM freed at once), then
+    // TMA reduce-add into the fp32 accumulator, 16 columns per box
+    auto drain = [&](uint32_t c, int blk, int bh) -> bool {
+      if (!wwait(bar(B_DQ_FULL), c & 1)) return false;
+      tc_fence_after();
+      uint32_t o[kDrainCols];
+#pragma unroll
+      for (int cc = 0; cc < kDrainCols / 32; ++cc)
+        tmem_ld32(tbase + lrow + C::kTmemDP + kDrainCols * h + 32 * cc,
+                  *reinterpret_cast<uint32_t(*)[32]>(&o[32 * cc]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_DQ_EMPTY));
+      const int qrow0 = blk * kBlk + 32 * quarter;     // first query row of this warp
+#pragma unroll
+      for (int cc = 0; cc < kDrainCols / 16; ++cc) {
+        if (lane == 0) bulk_wait_read_all();           // previous box has left the staging
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(strow + ((u ^ sw64) * 16)),
+                       "r"(o[16 * cc + 4 * u]), "r"(o[16 * cc + 4 * u + 1]),
+                       "r"(o[16 * cc + 4 * u + 2]), "r"(o[16 * cc + 4 * u + 3])
+                       : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && qrow0 < p.a.Nq) {             // boxes past Nq hold no rows
+          tma_reduce_add_3d(&tmDQ, stage, kDrainCols * h + 16 * cc, qrow0, bh);
+          bulk_commit_group();
+        }
+      }
+      return true;
+    };
     uint32_t qc = 0;
     int it = 0;
     bool ok = true;
@@ -315,167 +439,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       bwd_item(idx, p, bh, kb, first, count);
       const int key = kb * kBlk + r;
       const bool key_ok = key < p.a.Nkv;
+      // order per block b: dS_b, P_{b+1}, drain_b -- the next block's P is ready for its
+      // dV MMA before dQ_b has finished, and the reduce-add leaves the critical path
+      ok = p_phase(qc, block_at(first, 0, p), kb, key_ok, key);
       for (int ii = 0; ii < count && ok; ++ii, ++qc) {
         const int blk = block_at(first, ii, p);
-        const uint32_t st = qc & 1;
-        const float* sl = reinterpret_cast<const float*>(gbase + C::kOffLse + st * 512);
-        const float* sd = reinterpret_cast<const float*>(gbase + C::kOffDelta + st * 512);
-        // ---- P phase
-        ok = wwait(bar(B_Q_FULL0 + st), (qc >> 1) & 1) && wwait(bar(B_S_FULL), qc & 1);
-        if (!ok) break;
-        tc_fence_after();
-        const bool diag = p.a.causal && blk == kb;
-        const int q0 = blk * kBlk;
-        // P^T kept as bf16 pairs between the two phases (the values dV consumes); the
-        // register file allows 168 registers per thread with 10 warps per CTA
-        uint32_t Pp[64];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tmem_ld32(tbase + lrow + C::kTmemS + 32 * c, sr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(sl + 32 * c + i);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            float pv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              pv[e] = ex2f(fmaf(__uint_as_float(sr[i + e]), qk, -lv[e]));
-              if (!key_ok || (diag && q0 + 32 * c + i + e < key)) pv[e] = 0.f;
-            }
-            Pp[16 * c + i / 2] = pack_bf16x2(pv[0], pv[1]);
-            Pp[16 * c + i / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          }
-          tmem_st16(tbase + lrow + C::kTmemS + 16 * c,
-                    *reinterpret_cast<const uint32_t(*)[16]>(&Pp[16 * c]));
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(B_P_FULL));
-        // ---- dS phase
-        ok = wwait(bar(B_DP_FULL), qc & 1);
-        if (ok && qc > 0) ok = wwait(bar(B_DS_EMPTY), (qc - 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t dr[32];
-          tmem_ld32(tbase + lrow + C::kTmemDP + 32 * c, dr);
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(sd + 32 * c + i);
-            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float ds[4];
-            const uint32_t pa = Pp[16 * c + i / 2], pb = Pp[16 * c + i / 2 + 1];
-            const float pvv[4] = {__uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u),
-                                  __uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              ds[e] = pvv[e] * (__uint_as_float(dr[i + e]) - dv[e]);
-            pk[i / 2] = pack_bf16x2(ds[0], ds[1]);
-            pk[i / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
-          }
-          // queries [32c, 32c+32) = 16-byte units 4(c%2) .. 4(c%2)+3 of chunk c/2,
-          // each stored at its 128-byte-swizzled position (unit ^ row%8)
-          const uint32_t rowaddr = dsrow + (c >> 1) * C::kChunkBytes;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t unit = static_cast<uint32_t>(4 * (c & 1) + u) ^ sw;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowaddr + unit * 16),
-                         "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]),
-                         "r"(pk[4 * u + 3])
-                         : "memory");
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(B_DS_FULL));
+        ok = ds_phase(qc);
+        if (ok && ii + 1 < count) ok = p_phase(qc + 1, block_at(first, ii + 1, p), kb, key_ok, key);
+        if (ok) ok = drain(qc, blk, bh);
       }
       if (!ok) break;
-      // ---- epilogue: dV, dK rows of this item
+      // ---- epilogue: h = 0 stores dV, h = 1 stores dK for this item's key rows
       ok = wwait(bar(B_DKDV_FULL), it & 1);
       if (!ok) break;
       tc_fence_after();
       const size_t grow = (static_cast<size_t>(bh) * p.a.Nkv + (key_ok ? key : 0)) * D;
+      const uint32_t tcol = h ? C::kTmemDK : C::kTmemDV;
+      uint16_t* out = h ? p.a.dk : p.a.dv;
+      const float scale = h ? p.a.sm_scale : 1.0f;
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t tcol = half ? C::kTmemDK : C::kTmemDV;
-        uint16_t* out = half ? p.a.dk : p.a.dv;
-        const float scale = half ? p.a.sm_scale : 1.0f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tbase + lrow + tcol + 32 * c, o);
-          tmem_wait_ld();
-          uint32_t wv[16];
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tbase + lrow + tcol + 32 * c, ov);
+        tmem_wait_ld();
+        uint32_t wv[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            wv[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * scale,
-                                __uint_as_float(o[2 * i + 1]) * scale);
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + grow + 32 * c);
+        for (int i = 0; i < 16; ++i)
+          wv[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * scale,
+                              __uint_as_float(ov[2 * i + 1]) * scale);
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(out + grow + 32 * c);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
         }
       }
       tc_fence_before();
       mbar_arrive(bar(B_DKDV_EMPTY));
-    }
-  } else {
-    // ------------------------------------------------------------ dQ drain (query rows)
-    // Reads the whole dQ_b row from TMEM (one thread per query row), releases the TMEM
-    // columns at once, then adds the rows to the fp32 accumulator 32 columns at a time
-    // through a 128-byte-swizzled 4 KB staging box and a TMA bulk reduce-add (full
-    // 128-byte lines; rows beyond Nq are clipped by the tensor bounds).
-    const int quarter = warp & 3;
-    const uint32_t lrow = (32u * quarter) << 16;
-    const uint32_t stage = base + C::kOffStage + quarter * 4096;
-    const uint32_t srow = stage + lane * 128;
-    const uint32_t sw = static_cast<uint32_t>(lane & 7);
-    auto wwait = [&](uint32_t b_, uint32_t par) {
-      const bool okw = mbar_wait(b_, par, abort_flag, p.err);
-      return __all_sync(0xffffffffu, okw) != 0;
-    };
-    uint32_t qc = 0;
-    bool ok = true;
-    for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x) {
-      int bh, kb, first, count;
-      bwd_item(idx, p, bh, kb, first, count);
-      for (int ii = 0; ii < count; ++ii, ++qc) {
-        const int q0 = block_at(first, ii, p) * kBlk;
-        ok = wwait(bar(B_DQ_FULL), qc & 1);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t o[D];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-          tmem_ld32(tbase + lrow + C::kTmemDP + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * c]));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_DQ_EMPTY));
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          if (lane == 0) bulk_wait_read_all();  // the previous box has left the staging area
-          __syncwarp();
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + ((u ^ sw) * 16)),
-                         "r"(o[32 * c + 4 * u]), "r"(o[32 * c + 4 * u + 1]),
-                         "r"(o[32 * c + 4 * u + 2]), "r"(o[32 * c + 4 * u + 3])
-                         : "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && q0 + 32 * quarter < p.a.Nq) {  // boxes past Nq hold no rows
-            tma_reduce_add_3d(&tmDQ, stage, 32 * c, q0 + 32 * quarter, bh);
-            bulk_commit_group();
-          }
-        }
-      }
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
