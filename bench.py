@@ -46,6 +46,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The maximum of a per-rank time over all ranks (the job's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step_per_rank: float, steps: int, world: int,
+                     max_ms: float) -> float:
+    """Weak scaling: every rank runs its own workload; the job's throughput is all the
+    ranks' work divided by the slowest rank's time."""
+    return world * flops_per_step_per_rank * steps / (max_ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -256,13 +274,6 @@ def run_ours(args, w):
             tdist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        return float(t.item())
-
     # ---- device-resident timing
     for _ in range(args.warmup):
         fwd()
@@ -284,7 +295,7 @@ def run_ours(args, w):
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     fwd_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in ev)
     bwd_ms = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in ev)
     if capi.qat_attn_device_status(stream) != capi.Status.OK:
@@ -293,7 +304,7 @@ def run_ours(args, w):
     pairs = w.pairs
     flops_step = 16.0 * pairs * D
     ms_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, args.steps, world, total_ms)
 
     # ---- end to end: host buffers, copies inside the timed region
     hout = {}
@@ -328,8 +339,8 @@ def run_ours(args, w):
         e2e_step()
     s1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(s0.elapsed_time(s1))
-    e2e_value = (world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12) if e2e_steps else None
+    e2e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
+    e2e_value = whole_job_tflops(flops_step, e2e_steps, world, e2e_ms) if e2e_steps else None
 
     # ---- roofline of the dominant kernel work (the backward call)
     peaks, peak_src = load_peaks()
