@@ -64,6 +64,21 @@ def whole_job_tflops(flops_per_step_per_rank: float, steps: int, world: int,
     return world * flops_per_step_per_rank * steps / (max_ms * 1e-3) / 1e12
 
 
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` at the benchmarked workload, from the committed
+    ncu summary, or None when the kernel's source has changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "roofline_traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                return None
+        return rec["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -364,7 +379,9 @@ def run_ours(args, w):
         "roofline": {
             "kernel": "qat_attn_bwd call (prep + attn_bwd_tc_kernel + dQ convert)",
             "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
-            "frac": bwd_tf / peak_sus, "traffic": None,
+            "frac": bwd_tf / peak_sus,
+            "traffic": kernel_traffic("attn_bwd_tc_kernel") if w.name == WORKLOAD else None,
+            "traffic_unit": "bytes per launch of attn_bwd_tc_kernel (DRAM read + write)",
             "peak_kind": f"bf16_tflops_sustained ({peak_src})",
             "algorithmic_flops_per_launch": 10.0 * pairs * D,
         },
