@@ -316,8 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t dsrow = base + C::kOffDS + h * C::kChunkBytes + r * 128;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
     const uint32_t stage = base + C::kOffStage + (warp - 2) * 2048;
-    const uint32_t strow = stage + lane * 64;
-    const uint32_t sw64 = static_cast<uint32_t>((lane >> 1) & 3);
     constexpr int kDrainCols = D / 2;
     uint32_t Pp[32];                                  // P^T of the current block, bf16 pairs
     // P phase of block `blk` (global index c): P^T -> TMEM for the dV MMA
@@ -399,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     // drain of block c: this group's dQ columns out of TMEM (TMEM freed at once), then
-    // TMA reduce-add into the fp32 accumulator, 16 columns per box
+    // TMA reduce-add into the fp32 accumulator, 16 rows x 32 columns per box
     auto drain = [&](uint32_t c, int blk, int bh) -> bool {
       if (!wwait(bar(B_DQ_FULL), c & 1)) return false;
       tc_fence_after();
@@ -412,21 +410,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(B_DQ_EMPTY));
       const int qrow0 = blk * kBlk + 32 * quarter;     // first query row of this warp
+      // boxes of 16 rows x 32 columns (128-byte rows, 128-byte swizzle): the TMA cost
+      // grows with the number of row segments, so wide rows halve it against 64 bytes
 #pragma unroll
-      for (int cc = 0; cc < kDrainCols / 16; ++cc) {
-        if (lane == 0) bulk_wait_read_all();           // previous box has left the staging
-        __syncwarp();
+      for (int cc = 0; cc < kDrainCols / 32; ++cc) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(strow + ((u ^ sw64) * 16)),
-                       "r"(o[16 * cc + 4 * u]), "r"(o[16 * cc + 4 * u + 1]),
-                       "r"(o[16 * cc + 4 * u + 2]), "r"(o[16 * cc + 4 * u + 3])
-                       : "memory");
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && qrow0 < p.a.Nq) {             // boxes past Nq hold no rows
-          tma_reduce_add_3d(&tmDQ, stage, kDrainCols * h + 16 * cc, qrow0, bh);
-          bulk_commit_group();
+        for (int rh = 0; rh < 2; ++rh) {
+          if (lane == 0) bulk_wait_read_all();         // previous box has left the staging
+          __syncwarp();
+          if ((lane >> 4) == rh) {                     // the 16 lanes that own these rows
+            const uint32_t row = stage + (lane & 15) * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                           ::"r"(row + ((u ^ (lane & 7)) * 16)),
+                           "r"(o[32 * cc + 4 * u]), "r"(o[32 * cc + 4 * u + 1]),
+                           "r"(o[32 * cc + 4 * u + 2]), "r"(o[32 * cc + 4 * u + 3])
+                           : "memory");
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0 && qrow0 + 16 * rh < p.a.Nq) {  // boxes past Nq hold no rows
+            tma_reduce_add_3d(&tmDQ, stage, kDrainCols * h + 32 * cc, qrow0 + 16 * rh, bh);
+            bulk_commit_group();
+          }
         }
       }
       return true;

@@ -30,7 +30,7 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int D) {
 // [BH, N, D] bf16 viewed as a 3-D TMA tensor (D innermost), 64 x 128 x 1 boxes,
 // 128-byte swizzle, zero fill out of bounds.
 bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH);
-// [BH, N, D] fp32 as a 3-D TMA tensor with 16 x 32 x 1 boxes (64-byte rows, swizzled).
+// [BH, N, D] fp32 as a 3-D TMA tensor with 32 x 16 x 1 boxes (128-byte rows, swizzled).
 bool make_f32_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH);
 
 // Arguments of one forward launch (device pointers, validated by the ABI layer).
