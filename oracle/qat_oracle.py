@@ -132,6 +132,7 @@ def f32_to_bf16_rn(x) -> np.ndarray:
 
 def quant_tiles_fp32(p) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """Fake-quantize fp32 tiles row by row: p has shape [rows, cols] (one tile per row).
+    amax is the largest magnitude, so signed data (Q, K, V) use the same rule as P.
 
     Returns (deq float32 [rows, cols] = bf16-rounded quantized values,
              scale float32 [rows] = amax / 448,
@@ -139,7 +140,7 @@ def quant_tiles_fp32(p) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     All arithmetic is IEEE float32 with round-to-nearest, as the rule states.
     """
     p = np.ascontiguousarray(p, dtype=np.float32)
-    amax = p.max(axis=1)
+    amax = np.abs(p).max(axis=1)
     nz = amax > 0
     safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
     inv = (np.float32(E4M3_MAX) / safe).astype(np.float32)
@@ -313,3 +314,59 @@ def head_backward_sampled(q, k, v, do, sm_scale: float, causal: bool,
     ds = p * (do[q_rows] @ v.T - delta[q_rows][:, None])
     dq = sm_scale * (ds @ k)
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Q / K / V fake quantization and smooth_k (the page's IS_QAT input path)
+# ---------------------------------------------------------------------------
+# Sources: "attn_qat_train.py", _attention.forward: with IS_QAT the inputs are replaced
+# by fake-quantized copies (fake_quantize_q with BLOCK_M = 32 tokens, fake_quantize_kv
+# with BLOCK_N = 32 tokens, one program per 32-token block of one (batch, head)), the
+# backward uses those copies (use_qat_qkv_backward), and smooth_k first subtracts
+# k.mean(dim=(0, 1, 2)), the per-channel mean over batch, heads and tokens.
+# Readings (quant_utils is not on the pages): one FP8 E4M3 absmax scale per 32-token x D
+# block, tokens beyond N excluded; the smoothed value is fl32(k - mean) and is quantized
+# directly (no intermediate bf16 rounding); the stored result is bf16.
+
+QKV_TOKEN_BLOCK = 32
+
+
+def fake_quant_tokens_fp32(x, mean=None):
+    """fp32 rule for one head: x [N, D] (float32 values), optional fp32 mean [D] subtracted
+    first; one scale per 32-token block over all D values.  Returns (out float32 values
+    of the bf16 result [N, D], scales float32 [ceil(N/32)], codes uint8 [N, D])."""
+    x = np.asarray(x, dtype=np.float32)
+    if mean is not None:
+        x = (x - np.asarray(mean, dtype=np.float32)[None, :]).astype(np.float32)
+    n, d = x.shape
+    nb = (n + QKV_TOKEN_BLOCK - 1) // QKV_TOKEN_BLOCK
+    out = np.zeros((n, d), np.float32)
+    codes = np.zeros((n, d), np.uint8)
+    scales = np.zeros(nb, np.float32)
+    for b in range(nb):
+        lo, hi = b * QKV_TOKEN_BLOCK, min(n, (b + 1) * QKV_TOKEN_BLOCK)
+        deq, sc, cd = quant_tiles_fp32(x[lo:hi].reshape(1, -1))
+        out[lo:hi] = deq.reshape(hi - lo, d)
+        codes[lo:hi] = cd.reshape(hi - lo, d)
+        scales[b] = sc[0]
+    return out, scales, codes
+
+
+def fake_quant_tokens_exact(x):
+    """Exact-arithmetic form for one head (fp64): per 32-token block,
+    value = E4M3(448 x / amax) amax / 448 (zero block -> zero)."""
+    x = np.asarray(x, np.float64)
+    out = np.zeros_like(x)
+    for lo in range(0, x.shape[0], QKV_TOKEN_BLOCK):
+        blk = x[lo:lo + QKV_TOKEN_BLOCK]
+        amax = np.abs(blk).max()
+        if amax > 0:
+            _, c = e4m3_rne_satfinite(448.0 * blk / amax)
+            out[lo:lo + QKV_TOKEN_BLOCK] = c * amax / 448.0
+    return out
+
+
+def channel_mean(x):
+    """smooth_k's offset: the mean of x [B, H, N, D] over B, H and N, per channel (fp64)."""
+    x = np.asarray(x, np.float64)
+    return x.reshape(-1, x.shape[-1]).mean(axis=0)

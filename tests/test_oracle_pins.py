@@ -301,3 +301,61 @@ def test_backward_sampled_equals_full():
         m, l = orc.head_row_stats(q, k, 0.35, causal, row_chunk=13)
         f = orc.head_forward(q, k, v, 0.35, causal, quant=False)
         assert np.allclose(f["m"], m) and np.allclose(f["l"], l)
+
+
+# ---------------------------------------------------------------- Q/K/V fake quantization
+
+def _nearest_signed(x):
+    c, v = nearest_e4m3(abs(x))
+    return (c | 0x80, -v) if (x < 0 and v > 0) else (c, v)
+
+
+def test_qkv_fake_quant_matches_scalar_loop():
+    rng = np.random.default_rng(50)
+    x = (rng.standard_normal((70, 8)) * 3).astype(np.float32)      # 3 blocks, ragged tail
+    x[40:64] = 0.0                                                   # an all-zero block
+    mean = (rng.standard_normal(8) * 2).astype(np.float32)
+    out, scales, codes = orc.fake_quant_tokens_fp32(x, mean)
+    xs = (x - mean[None, :]).astype(np.float32)
+    for b in range(3):
+        blk = xs[32 * b:32 * b + 32]
+        amax = np.float32(np.abs(blk).max())
+        inv = np.float32(448.0) / amax
+        s = amax / np.float32(448.0)
+        assert scales[b] == s
+        for (i, j), val in np.ndenumerate(blk):
+            wc, wv = _nearest_signed(float(np.float32(val * inv)))
+            assert codes[32 * b + i, j] == wc
+            assert out[32 * b + i, j] == _bf16_rn_scalar(np.float32(np.float32(wv) * s))
+
+
+def test_qkv_fake_quant_invariants():
+    rng = np.random.default_rng(51)
+    x = (rng.standard_normal((96, 16)) * 2).astype(np.float32)
+    out, scales, codes = orc.fake_quant_tokens_fp32(x)
+    o2, s2, c2 = orc.fake_quant_tokens_fp32(-x)                     # sign symmetry
+    assert np.array_equal(o2, -out) and np.array_equal(s2, scales)
+    assert np.array_equal(c2 & 0x7F, codes & 0x7F)
+    o3, s3, c3 = orc.fake_quant_tokens_fp32(x * np.float32(8.0))    # scale invariance
+    assert np.array_equal(c3, codes) and np.array_equal(o3, out * np.float32(8.0))
+    for b in range(3):                                               # block max -> +-448
+        blk = np.abs(x[32 * b:32 * b + 32])
+        i, j = np.unravel_index(np.argmax(blk), blk.shape)
+        assert codes[32 * b + i, j] & 0x7F == 0x7E
+    _, _, c4 = orc.fake_quant_tokens_fp32(out)                       # idempotent codes
+    assert np.array_equal(c4, codes)
+    exact = orc.fake_quant_tokens_exact(x.astype(np.float64))
+    assert np.allclose(out, exact, rtol=2 ** -7, atol=0)             # bf16 rounding only
+
+
+def test_smooth_k_is_a_softmax_shift():
+    """Subtracting the per-channel K mean shifts each score row by a constant, so the
+    unquantized outputs and the normalized P are unchanged."""
+    q, k, v = rng_f64(52, 2, 3, 40, 8), rng_f64(53, 2, 3, 40, 8), rng_f64(54, 2, 3, 40, 8)
+    k = k + np.array([5.0, -3.0, 0.5, 9.0, 0.0, -7.0, 2.0, 1.0])
+    mu = orc.channel_mean(k)
+    assert np.allclose(mu, k.mean(axis=(0, 1, 2)))
+    assert np.allclose(orc.channel_mean(k - mu), 0.0, atol=1e-12)
+    a = orc.forward(q, k, v, 0.3, False, quant=False)
+    b = orc.forward(q, k - mu, v, 0.3, False, quant=False)
+    assert np.allclose(a[1], b[1], rtol=1e-11, atol=1e-12)
