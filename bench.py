@@ -357,6 +357,36 @@ def run_ours(args, w):
     e2e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
     e2e_value = whole_job_tflops(flops_step, e2e_steps, world, e2e_ms) if e2e_steps else None
 
+    # ---- the Q/K/V fake-quantization row (HBM-bound): channel mean of K + 3 passes
+    qkv = None
+    if w.name == WORKLOAD:
+        fq = [torch.empty_like(x[n]) for n in ("q", "k", "v")]
+        kmean = torch.empty(D, dtype=torch.float32, device=dev)
+
+        def qkv_pass():
+            capi.qat_channel_mean(x["k"], kmean, B, H, Nkv, D, stream)
+            capi.qat_fake_quant_tokens(x["q"], None, fq[0], None, B, H, Nq, D, stream)
+            capi.qat_fake_quant_tokens(x["k"], kmean, fq[1], None, B, H, Nkv, D, stream)
+            capi.qat_fake_quant_tokens(x["v"], None, fq[2], None, B, H, Nkv, D, stream)
+
+        for _ in range(3):
+            qkv_pass()
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        q0.record(stream)
+        for _ in range(10):
+            qkv_pass()
+        q1.record(stream)
+        barrier()
+        qkv_ms = q0.elapsed_time(q1) / 10
+        elem = 2  # bf16
+        qkv_bytes = elem * (B * H * Nkv * D                       # K read for the mean
+                            + 2 * (B * H * Nq * D + 2 * B * H * Nkv * D))  # 3 x (read + write)
+        qkv = {"ms": qkv_ms, "bytes": qkv_bytes, "gbs": qkv_bytes / (qkv_ms * 1e-3) / 1e9,
+               "what": "qat_channel_mean(K) + qat_fake_quant_tokens(Q, K - mean, V) at c4"}
+        del fq
+
     # ---- roofline of the dominant kernel work (the backward call)
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -388,6 +418,8 @@ def run_ours(args, w):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
+        "next_rows": {"qkv_fake_quant": dict(qkv, frac_of_hbm=qkv["gbs"] / float(
+            peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))) if qkv else None},
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

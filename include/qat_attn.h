@@ -146,6 +146,37 @@ QAT_API qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const vo
                           int B, int H, int Nq, int Nkv, int D,
                           float sm_scale, int causal, int quant_mode, void* stream);
 
+/*
+ * qat_channel_mean -- smooth_k's offset: mean[c] = mean of x[b, h, n, c] over b, h and n.
+ *   ("attn_qat_train.py", _attention.forward: k.mean(dim=(0, 1, 2)).)
+ *   x     bf16 [B, H, N, D] (device)
+ *   mean  fp32 [D] (device) OUT.  Summed with fp32 atomics, so its last bits may vary
+ *         from run to run.
+ *   D 64 or 128; B, H, N >= 0 (an empty x gives mean = 0).
+ * Errors: QAT_ERR_INVALID_ARG (null / misaligned pointer, bad size or D), QAT_ERR_CUDA.
+ */
+QAT_API qat_status_t qat_channel_mean(const void* x, float* mean, int B, int H, int N, int D,
+                                      void* stream);
+
+/*
+ * qat_fake_quant_tokens -- fake-quantizes Q, K or V to FP8 E4M3 with one absmax scale
+ * per (head, 32-token block) over all D channels, as the page's IS_QAT path does before
+ * attention.  ("attn_qat_train.py", _attention.forward: fake_quantize_q with
+ * BLOCK_M = 32, fake_quantize_kv with BLOCK_N = 32.)
+ *   x       bf16 [B, H, N, D] (device)
+ *   mean    fp32 [D] or NULL: subtracted from every token first (smooth_k for K)
+ *   out     bf16 [B, H, N, D] OUT (may be x itself)
+ *   scales  fp32 [B, H, ceil(N / 32)] OUT or NULL: amax / 448 per block
+ *   Rule per block: x' = fl32(x - mean), amax = max |x'|,
+ *   code = E4M3_RNE_SATFINITE(fl32(x' * fl32(448 / amax))),
+ *   out = bf16(fl32(decode(code) * fl32(amax / 448))); an all-zero block stays zero.
+ *   Tokens beyond N are excluded.
+ * Errors: QAT_ERR_INVALID_ARG (null / misaligned x or out, bad size or D), QAT_ERR_CUDA.
+ */
+QAT_API qat_status_t qat_fake_quant_tokens(const void* x, const float* mean, void* out,
+                                           float* scales, int B, int H, int N, int D,
+                                           void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 QAT_API const char* qat_status_string(qat_status_t status);
 

@@ -8,4 +8,4 @@ and fails loudly if it has not been built.
 
 from .capi import QUANT_NONE, QUANT_P_FP8E4M3_ROW_TILE64, QatError, Status  # noqa: F401
 from .attention import (QATAttention, attention, qat_attention_backward,  # noqa: F401
-                        qat_attention_forward)
+                        qat_attention_forward, qat_prepare_qkv)

@@ -85,13 +85,36 @@ def qat_attention_backward(q, k, v, o_hp, lse, do, causal: bool = False,
     return dq, dk, dv
 
 
+def qat_prepare_qkv(q, k, v, smooth_k: bool = True):
+    """The page's IS_QAT inputs: fake-quantized copies of q, k, v (FP8 E4M3, one absmax
+    scale per (head, 32-token block)); with smooth_k the per-channel mean of K over
+    batch, heads and tokens is subtracted before K is quantized ("attn_qat_train.py",
+    _attention.forward).  Returns (q_fq, k_fq, v_fq, k_mean or None)."""
+    B, H, Nq, Nkv, D = _dims(q, k, v)
+    k_mean = None
+    with torch.cuda.device(q.device):
+        if smooth_k:
+            k_mean = torch.empty(D, dtype=torch.float32, device=q.device)
+            _raise(capi.qat_channel_mean(k, k_mean, B, H, Nkv, D), "qat_channel_mean")
+        out = []
+        for x, n, m in ((q, Nq, None), (k, Nkv, k_mean), (v, Nkv, None)):
+            y = torch.empty_like(x)
+            _raise(capi.qat_fake_quant_tokens(x, m, y, None, B, H, n, D), "qat_fake_quant_tokens")
+            out.append(y)
+    return out[0], out[1], out[2], k_mean
+
+
 class QATAttention(torch.autograd.Function):
     """Forward returns O_q; backward returns dq, dk, dv through the straight-through
     estimator (gradients of O_hp)."""
 
     @staticmethod
     def forward(ctx, q, k, v, causal=False, sm_scale=None,
-                quant_mode=capi.QUANT_P_FP8E4M3_ROW_TILE64):
+                quant_mode=capi.QUANT_P_FP8E4M3_ROW_TILE64, qkv_quant=False, smooth_k=False):
+        if qkv_quant:  # attention runs on fake-quantized inputs; gradients pass straight
+            q, k, v, _ = qat_prepare_qkv(q, k, v, smooth_k)
+        elif smooth_k:
+            raise ValueError("smooth_k changes the result only together with qkv_quant")
         o_q, o_hp, lse = qat_attention_forward(q, k, v, causal, sm_scale, quant_mode)
         ctx.save_for_backward(q, k, v, o_hp, lse)
         ctx.causal, ctx.sm_scale, ctx.quant_mode = causal, sm_scale, quant_mode
@@ -102,10 +125,13 @@ class QATAttention(torch.autograd.Function):
         q, k, v, o_hp, lse = ctx.saved_tensors
         dq, dk, dv = qat_attention_backward(q, k, v, o_hp, lse, do.contiguous(), ctx.causal,
                                             ctx.sm_scale, ctx.quant_mode)
-        return dq, dk, dv, None, None, None
+        return dq, dk, dv, None, None, None, None, None
 
 
 def attention(q, k, v, causal: bool = False, sm_scale: float | None = None,
-              quant_mode: int = capi.QUANT_P_FP8E4M3_ROW_TILE64):
-    """QAT attention: the quantized output O_q, differentiable (straight-through)."""
-    return QATAttention.apply(q, k, v, causal, sm_scale, quant_mode)
+              quant_mode: int = capi.QUANT_P_FP8E4M3_ROW_TILE64, qkv_quant: bool = False,
+              smooth_k: bool = False):
+    """QAT attention: the quantized output O_q, differentiable (straight-through).
+    qkv_quant additionally fake-quantizes q, k, v per 32-token block first (the page's
+    full IS_QAT path), smooth_k subtracting K's channel mean before K is quantized."""
+    return QATAttention.apply(q, k, v, causal, sm_scale, quant_mode, qkv_quant, smooth_k)

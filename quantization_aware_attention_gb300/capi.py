@@ -25,6 +25,8 @@ EXPORTED = (
     "qat_status_string",
     "qat_attn_device_status",
     "qat_debug_quant_tiles",
+    "qat_channel_mean",
+    "qat_fake_quant_tokens",
 )
 
 
@@ -74,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.qat_attn_device_status.restype = _i
         L.qat_debug_quant_tiles.argtypes = [_vp, _i, _i, _vp, _vp, _vp, _vp]
         L.qat_debug_quant_tiles.restype = _i
+        L.qat_channel_mean.argtypes = [_vp, _vp] + [_i] * 4 + [_vp]
+        L.qat_channel_mean.restype = _i
+        L.qat_fake_quant_tokens.argtypes = [_vp] * 4 + [_i] * 4 + [_vp]
+        L.qat_fake_quant_tokens.restype = _i
         _lib = L
     return _lib
 
@@ -133,3 +139,12 @@ def qat_attn_device_status(stream=None) -> Status:
 def qat_debug_quant_tiles(p, rows, cols, deq, scales, codes, stream=None) -> Status:
     return Status(lib().qat_debug_quant_tiles(_ptr(p), rows, cols, _ptr(deq), _ptr(scales),
                                               _ptr(codes), _stream(stream)))
+
+
+def qat_channel_mean(x, mean, B, H, N, D, stream=None) -> Status:
+    return Status(lib().qat_channel_mean(_ptr(x), _ptr(mean), B, H, N, D, _stream(stream)))
+
+
+def qat_fake_quant_tokens(x, mean, out, scales, B, H, N, D, stream=None) -> Status:
+    return Status(lib().qat_fake_quant_tokens(_ptr(x), _ptr(mean), _ptr(out), _ptr(scales), B, H,
+                                              N, D, _stream(stream)))

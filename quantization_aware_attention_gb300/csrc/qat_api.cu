@@ -64,7 +64,6 @@ constexpr long long kMaxRows = 2147483647LL;  // rows of a [B*H*N, D] view
 constexpr int kMaxBH = 65535;                   // grid y dimension
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Checks shared by the forward and backward entry points.  Sets *empty when there is
 // no query work (B, H or Nq is zero).
@@ -207,6 +206,37 @@ qat_status_t qat_attn_device_status(void* stream) {
   const cudaError_t e = qat::read_and_clear_device_error(&word, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QAT_ERR_CUDA;
   return word ? QAT_ERR_TIMEOUT : QAT_OK;
+}
+
+qat_status_t qat_channel_mean(const void* x, float* mean, int B, int H, int N, int D,
+                              void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128)) return QAT_ERR_INVALID_ARG;
+  if (mean == nullptr || (reinterpret_cast<uintptr_t>(mean) & 3u) != 0) return QAT_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows > kMaxRows) return QAT_ERR_INVALID_ARG;
+  if (rows > 0 && (x == nullptr || !aligned16(x))) return QAT_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int num_sms = 0;
+  cudaError_t e = qat::device_context(&err, &num_sms);
+  if (e == cudaSuccess)
+    e = qat::launch_channel_mean(static_cast<const uint16_t*>(x), mean, rows, D, num_sms,
+                                 static_cast<cudaStream_t>(stream));
+  return from_cuda(e);
+}
+
+qat_status_t qat_fake_quant_tokens(const void* x, const float* mean, void* out, float* scales,
+                                   int B, int H, int N, int D, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128)) return QAT_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * N > kMaxRows || bh * ((N + 31) / 32) > kMaxRows) return QAT_ERR_INVALID_ARG;
+  if (bh * N == 0) return QAT_OK;
+  if (x == nullptr || out == nullptr || !aligned16(x) || !aligned16(out)) return QAT_ERR_INVALID_ARG;
+  if (mean != nullptr && (reinterpret_cast<uintptr_t>(mean) & 3u) != 0) return QAT_ERR_INVALID_ARG;
+  if (scales != nullptr && (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return QAT_ERR_INVALID_ARG;
+  return from_cuda(qat::launch_fake_quant_tokens(
+      static_cast<const uint16_t*>(x), mean, static_cast<uint16_t*>(out), scales,
+      static_cast<int>(bh), N, D, static_cast<cudaStream_t>(stream)));
 }
 
 qat_status_t qat_debug_quant_tiles(const float* p, int rows, int cols, float* deq, float* scales,

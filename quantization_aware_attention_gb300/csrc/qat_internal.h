@@ -71,6 +71,10 @@ struct BwdArgs {
 // Kernel launchers (return cudaGetLastError() after the launches).
 cudaError_t launch_fwd_tc(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
+cudaError_t launch_channel_mean(const uint16_t* x, float* mean, long long rows, int D,
+                                int num_sms, cudaStream_t s);
+cudaError_t launch_fake_quant_tokens(const uint16_t* x, const float* mean, uint16_t* out,
+                                     float* scales, int BH, int N, int D, cudaStream_t s);
 cudaError_t launch_debug_quant(const float* p, int rows, int cols, float* deq,
                                float* scales, uint8_t* codes, cudaStream_t s);
 
