@@ -370,3 +370,29 @@ def channel_mean(x):
     """smooth_k's offset: the mean of x [B, H, N, D] over B, H and N, per channel (fp64)."""
     x = np.asarray(x, np.float64)
     return x.reshape(-1, x.shape[-1]).mean(axis=0)
+
+
+# ---------------------------------------------------------------------------
+# Partial results over key chunks and their merge (ring / context-parallel block)
+# ---------------------------------------------------------------------------
+# A forward over keys [c0, c1) of each head gives O_q, O_hp (each normalized by its own
+# l) and lse (base 2).  Two partials over disjoint key sets merge exactly:
+#   lse = log2(2^lse_a + 2^lse_b),  O = 2^(lse_a - lse) O_a + 2^(lse_b - lse) O_b
+# for O_hp; for O_q the same holds when every chunk starts at a multiple of 64 keys, so
+# each 64-key quantization tile lies inside one chunk (the per-tile codes and amax are
+# then the same as in a one-pass forward, and O_q carries the same weights as O_hp).
+# Source of the setting: "usp: differentiable operators for training (Ulysses/Ring/local
+# attention)" (ring attention passes partial outputs between ranks and merges them).
+
+def merge_partials(o_a, lse_a, o_b, lse_b):
+    """Merge two partial attention results (fp64): o [..., rows, D], lse [..., rows]."""
+    lse_a = np.asarray(lse_a, np.float64)
+    lse_b = np.asarray(lse_b, np.float64)
+    hi = np.maximum(lse_a, lse_b)
+    hi = np.where(np.isfinite(hi), hi, 0.0)
+    wa = np.exp2(lse_a - hi)
+    wb = np.exp2(lse_b - hi)
+    lse = hi + np.log2(wa + wb)
+    tot = wa + wb
+    o = (wa[..., None] * np.asarray(o_a, np.float64) + wb[..., None] * np.asarray(o_b, np.float64))
+    return o / tot[..., None], lse

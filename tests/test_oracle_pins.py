@@ -359,3 +359,50 @@ def test_smooth_k_is_a_softmax_shift():
     a = orc.forward(q, k, v, 0.3, False, quant=False)
     b = orc.forward(q, k - mu, v, 0.3, False, quant=False)
     assert np.allclose(a[1], b[1], rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- key-chunk partials and merge
+
+@pytest.mark.parametrize("cuts", [(64,), (128, 192), (64, 128, 256)])
+def test_merge_of_chunks_equals_one_pass(cuts):
+    """Forward over key chunks starting at multiples of 64, merged by lse, equals the
+    one-pass forward for O_hp, lse and O_q (the quantization tiles stay whole)."""
+    n, d = 300, 8
+    q, k, v = rng_f64(60, 1, 2, 20, d), rng_f64(61, 1, 2, n, d), rng_f64(62, 1, 2, n, d)
+    full = orc.forward(q, k, v, 0.4, False, quant=True)
+    edges = (0,) + tuple(cuts) + (n,)
+    acc_q = acc_h = acc_l = None
+    for lo, hi in zip(edges[:-1], edges[1:]):
+        oq, oh, lse = orc.forward(q, k[:, :, lo:hi], v[:, :, lo:hi], 0.4, False, quant=True)
+        if acc_l is None:
+            acc_q, acc_h, acc_l = oq, oh, lse
+        else:
+            acc_q, _ = orc.merge_partials(acc_q, acc_l, oq, lse)
+            acc_h, acc_l = orc.merge_partials(acc_h, acc_l, oh, lse)
+    assert np.allclose(acc_h, full[1], rtol=1e-12, atol=1e-13)
+    assert np.allclose(acc_l, full[2], rtol=1e-12, atol=1e-13)
+    assert np.allclose(acc_q, full[0], rtol=1e-12, atol=1e-13)
+
+
+def test_merge_identity_and_symmetry():
+    o = rng_f64(63, 5, 4)
+    lse = rng_f64(64, 5)
+    o2, l2 = orc.merge_partials(o, lse, rng_f64(65, 5, 4), np.full(5, -np.inf))
+    assert np.allclose(o2, o) and np.allclose(l2, lse)
+    a = orc.merge_partials(o, lse, o * 2, lse + 1)
+    b = orc.merge_partials(o * 2, lse + 1, o, lse)
+    assert np.allclose(a[0], b[0]) and np.allclose(a[1], b[1])
+
+
+def test_chunk_not_aligned_to_quant_tiles_differs():
+    """A cut inside a 64-key tile splits that tile's quantization, so O_q changes (this
+    is why chunked calls require starts at multiples of 64); O_hp still merges."""
+    n, d = 200, 8
+    q, k, v = rng_f64(66, 1, 1, 10, d, scale=2.0), rng_f64(67, 1, 1, n, d), rng_f64(68, 1, 1, n, d)
+    full = orc.forward(q, k, v, 0.6, False, quant=True)
+    a = orc.forward(q, k[:, :, :100], v[:, :, :100], 0.6, False, quant=True)
+    b = orc.forward(q, k[:, :, 100:], v[:, :, 100:], 0.6, False, quant=True)
+    oh, _ = orc.merge_partials(a[1], a[2], b[1], b[2])
+    oq, _ = orc.merge_partials(a[0], a[2], b[0], b[2])
+    assert np.allclose(oh, full[1], rtol=1e-12)
+    assert not np.allclose(oq, full[0], rtol=1e-9)
