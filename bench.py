@@ -46,6 +46,10 @@ def dist_env():
     return world, rank, local
 
 
+def pairs_of(w) -> int:
+    return w.pairs
+
+
 def max_over_ranks(value: float, world: int, device=None) -> float:
     """The maximum of a per-rank time over all ranks (the job's time)."""
     if world == 1:
@@ -387,6 +391,44 @@ def run_ours(args, w):
                "what": "qat_channel_mean(K) + qat_fake_quant_tokens(Q, K - mean, V) at c4"}
         del fq
 
+    # ---- the key-chunk forward + merge row: c4 as 4 chunks of Nkv / 4 keys
+    chunked = None
+    if w.name == WORKLOAD:
+        nch = 4
+        clen = Nkv // nch
+        acc = [torch.empty(B, H, Nq, D, device=dev), torch.empty(B, H, Nq, D, device=dev),
+               torch.empty(B, H, Nq, device=dev)]
+        part = [torch.empty_like(acc[0]), torch.empty_like(acc[1]), torch.empty_like(acc[2])]
+        quant = capi.QUANT_P_FP8E4M3_ROW_TILE64
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+        def chunked_pass():
+            capi.qat_attn_fwd_chunk(x["q"], x["k"], x["v"], *acc, B, H, Nq, Nkv, 0, clen, D, sm,
+                                    quant, stream)
+            for c in range(1, nch):
+                capi.qat_attn_fwd_chunk(x["q"], x["k"], x["v"], *part, B, H, Nq, Nkv, c * clen,
+                                        clen, D, sm, quant, stream)
+                capi.qat_attn_merge(*acc, *part, o_q if c == nch - 1 else None,
+                                    o_hp if c == nch - 1 else None, B, H, Nq, D, stream)
+
+        chunked_pass()
+        barrier()
+        ev[0].record(stream)
+        chunked_pass()
+        ev[1].record(stream)
+        for c in range(1, nch):
+            capi.qat_attn_merge(*acc, *part, None, None, B, H, Nq, D, stream)
+        ev[2].record(stream)
+        barrier()
+        ch_ms = ev[0].elapsed_time(ev[1])
+        merge_ms = ev[1].elapsed_time(ev[2]) / (nch - 1)
+        merge_bytes = 4 * B * H * Nq * (4 * D + 3)  # read acc + part, write acc (O_q, O_hp, lse)
+        chunked = {"chunks": nch, "ms": ch_ms, "tflops": 6.0 * pairs_of(w) * D / (ch_ms * 1e-3) / 1e12,
+                   "one_pass_fwd_ms": None, "merge_ms": merge_ms,
+                   "merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9,
+                   "what": "c4 forward as 4 key chunks (fp32 partials) + 3 lse merges"}
+        del acc, part
+
     # ---- roofline of the dominant kernel work (the backward call)
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -418,8 +460,10 @@ def run_ours(args, w):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
-        "next_rows": {"qkv_fake_quant": dict(qkv, frac_of_hbm=qkv["gbs"] / float(
-            peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))) if qkv else None},
+        "next_rows": {
+            "qkv_fake_quant": dict(qkv, frac_of_hbm=qkv["gbs"] / float(
+                peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))) if qkv else None,
+            "kv_chunk_merge": dict(chunked, one_pass_fwd_ms=fwd_ms) if chunked else None},
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

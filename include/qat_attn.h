@@ -147,6 +147,42 @@ QAT_API qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const vo
                           float sm_scale, int causal, int quant_mode, void* stream);
 
 /*
+ * qat_attn_fwd_chunk -- forward over one chunk of keys, returning a partial result to be
+ * merged with qat_attn_merge: the single-GPU building block of ring / context-parallel
+ * attention ("usp: differentiable operators for training (Ulysses/Ring/local attention)":
+ * ring attention rotates K/V chunks and merges partial outputs).
+ *   q           bf16 [B, H, Nq, D]
+ *   k, v        bf16 [B, H, Nkv_total, D]; keys [kv_begin, kv_begin + kv_len) are used
+ *   o_q, o_hp   fp32 [B, H, Nq, D] OUT: the chunk's outputs, each normalized by the
+ *               chunk's own row sum
+ *   lse         fp32 [B, H, Nq] OUT: the chunk's base-2 log-sum-exp
+ *   Non-causal only.  kv_begin must be a multiple of 64 so that no quantization tile is
+ *   split between chunks; then merging all chunks reproduces the one-pass O_q exactly
+ *   in real arithmetic, as it does O_hp and lse.
+ * Errors: as qat_attn_fwd; QAT_ERR_INVALID_ARG for a chunk outside [0, Nkv_total);
+ *   QAT_ERR_UNSUPPORTED when kv_begin % 64 != 0.
+ */
+QAT_API qat_status_t qat_attn_fwd_chunk(const void* q, const void* k, const void* v,
+                                        float* o_q, float* o_hp, float* lse,
+                                        int B, int H, int Nq, int Nkv_total, int kv_begin,
+                                        int kv_len, int D, float sm_scale, int quant_mode,
+                                        void* stream);
+
+/*
+ * qat_attn_merge -- merges a partial result into an accumulator (both fp32, same
+ * layout as qat_attn_fwd_chunk's outputs), in place:
+ *   lse_acc <- log2(2^lse_acc + 2^lse_part)
+ *   O_acc   <- 2^(lse_acc_old - lse_acc) O_acc + 2^(lse_part - lse_acc) O_part
+ * for O_q and O_hp.  If o_q_out / o_hp_out (bf16 [B, H, Nq, D]) are not NULL, the merged
+ * outputs are also written there.  An lse of -inf marks an empty partial.
+ * Errors: QAT_ERR_INVALID_ARG (null / misaligned pointer, bad size or D), QAT_ERR_CUDA.
+ */
+QAT_API qat_status_t qat_attn_merge(float* o_q_acc, float* o_hp_acc, float* lse_acc,
+                                    const float* o_q_part, const float* o_hp_part,
+                                    const float* lse_part, void* o_q_out, void* o_hp_out,
+                                    int B, int H, int Nq, int D, void* stream);
+
+/*
  * qat_channel_mean -- smooth_k's offset: mean[c] = mean of x[b, h, n, c] over b, h and n.
  *   ("attn_qat_train.py", _attention.forward: k.mean(dim=(0, 1, 2)).)
  *   x     bf16 [B, H, N, D] (device)

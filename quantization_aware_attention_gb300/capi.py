@@ -27,6 +27,8 @@ EXPORTED = (
     "qat_debug_quant_tiles",
     "qat_channel_mean",
     "qat_fake_quant_tokens",
+    "qat_attn_fwd_chunk",
+    "qat_attn_merge",
 )
 
 
@@ -80,6 +82,10 @@ def lib() -> ctypes.CDLL:
         L.qat_channel_mean.restype = _i
         L.qat_fake_quant_tokens.argtypes = [_vp] * 4 + [_i] * 4 + [_vp]
         L.qat_fake_quant_tokens.restype = _i
+        L.qat_attn_fwd_chunk.argtypes = [_vp] * 6 + [_i] * 7 + [_f, _i, _vp]
+        L.qat_attn_fwd_chunk.restype = _i
+        L.qat_attn_merge.argtypes = [_vp] * 8 + [_i] * 4 + [_vp]
+        L.qat_attn_merge.restype = _i
         _lib = L
     return _lib
 
@@ -148,3 +154,18 @@ def qat_channel_mean(x, mean, B, H, N, D, stream=None) -> Status:
 def qat_fake_quant_tokens(x, mean, out, scales, B, H, N, D, stream=None) -> Status:
     return Status(lib().qat_fake_quant_tokens(_ptr(x), _ptr(mean), _ptr(out), _ptr(scales), B, H,
                                               N, D, _stream(stream)))
+
+
+def qat_attn_fwd_chunk(q, k, v, o_q, o_hp, lse, B, H, Nq, Nkv_total, kv_begin, kv_len, D,
+                       sm_scale, quant_mode, stream=None) -> Status:
+    return Status(lib().qat_attn_fwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(o_q), _ptr(o_hp),
+                                           _ptr(lse), B, H, Nq, Nkv_total, kv_begin, kv_len, D,
+                                           float(sm_scale), int(quant_mode), _stream(stream)))
+
+
+def qat_attn_merge(o_q_acc, o_hp_acc, lse_acc, o_q_part, o_hp_part, lse_part, o_q_out, o_hp_out,
+                   B, H, Nq, D, stream=None) -> Status:
+    return Status(lib().qat_attn_merge(_ptr(o_q_acc), _ptr(o_hp_acc), _ptr(lse_acc),
+                                       _ptr(o_q_part), _ptr(o_hp_part), _ptr(lse_part),
+                                       _ptr(o_q_out), _ptr(o_hp_out), B, H, Nq, D,
+                                       _stream(stream)))

@@ -416,11 +416,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t orow = (static_cast<size_t>(bh) * p.a.Nq + (in ? row : 0)) * D;
       const uint32_t tO = tbase + lrow + (h ? C::kTmemOhp : C::kTmemOq);
       uint16_t* out = h ? p.a.o_hp : p.a.o_q;
+      float* out32 = h ? p.a.o_hp_f32 : p.a.o_q_f32;  // partial results stay fp32
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
+        if (out32 != nullptr) {
+          if (in) {
+            float4* dst = reinterpret_cast<float4*>(out32 + orow + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          }
+          continue;
+        }
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -452,8 +463,9 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a, unsigned int* err, int num_sms, cu
   using C = FwdTc<D>;
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv;
-  if (!make_bf16_map_3d(&mq, a.q, D, a.Nq, BH) || !make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) ||
-      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH))
+  if (!make_bf16_map_3d(&mq, a.q, D, a.Nq, BH) ||
+      !make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH, a.kv_head_rows) ||
+      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH, a.kv_head_rows))
     return cudaErrorInvalidValue;
   TcParams p;
   p.a = a;
@@ -489,13 +501,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH) {
+bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH, int head_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
+  if (head_rows < 0) head_rows = N;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(N) * D * 2};
+                                 static_cast<cuuint64_t>(head_rows) * D * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,

@@ -137,10 +137,72 @@ qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v, void* o_q
   a.qk_scale = sm_scale * kLog2e;
   a.causal = causal;
   a.quant = quant_mode == QAT_QUANT_P_FP8E4M3_ROW_TILE64;
+  a.kv_head_rows = Nkv;
+  a.o_q_f32 = nullptr;
+  a.o_hp_f32 = nullptr;
   unsigned int* err = nullptr;
   int num_sms = 0;
   cudaError_t e = qat::device_context(&err, &num_sms);
   if (e == cudaSuccess) e = qat::launch_fwd_tc(a, err, num_sms, static_cast<cudaStream_t>(stream));
+  return from_cuda(e);
+}
+
+qat_status_t qat_attn_fwd_chunk(const void* q, const void* k, const void* v, float* o_q,
+                                float* o_hp, float* lse, int B, int H, int Nq, int Nkv_total,
+                                int kv_begin, int kv_len, int D, float sm_scale, int quant_mode,
+                                void* stream) {
+  bool empty = false;
+  const qat_status_t st = check_sizes(B, H, Nq, Nkv_total, D, sm_scale, 0, quant_mode, &empty);
+  if (st != QAT_OK || empty) return st;
+  if (kv_begin < 0 || kv_len < 1 || static_cast<long long>(kv_begin) + kv_len > Nkv_total)
+    return QAT_ERR_INVALID_ARG;
+  if (kv_begin % 64 != 0) return QAT_ERR_UNSUPPORTED;  // a quantization tile would be split
+  const void* ptrs[] = {q, k, v, o_q, o_hp, lse};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return QAT_ERR_INVALID_ARG;
+  const size_t off = static_cast<size_t>(kv_begin) * D;
+  qat::FwdArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k) + off;
+  a.v = static_cast<const uint16_t*>(v) + off;
+  a.o_q = nullptr;
+  a.o_hp = nullptr;
+  a.lse = lse;
+  a.B = B; a.H = H; a.Nq = Nq; a.Nkv = kv_len; a.D = D;
+  a.sm_scale = sm_scale;
+  a.qk_scale = sm_scale * kLog2e;
+  a.causal = 0;
+  a.quant = quant_mode == QAT_QUANT_P_FP8E4M3_ROW_TILE64;
+  a.kv_head_rows = Nkv_total;
+  a.o_q_f32 = o_q;
+  a.o_hp_f32 = o_hp;
+  unsigned int* err = nullptr;
+  int num_sms = 0;
+  cudaError_t e = qat::device_context(&err, &num_sms);
+  if (e == cudaSuccess) e = qat::launch_fwd_tc(a, err, num_sms, static_cast<cudaStream_t>(stream));
+  return from_cuda(e);
+}
+
+qat_status_t qat_attn_merge(float* o_q_acc, float* o_hp_acc, float* lse_acc,
+                            const float* o_q_part, const float* o_hp_part, const float* lse_part,
+                            void* o_q_out, void* o_hp_out, int B, int H, int Nq, int D,
+                            void* stream) {
+  if (B < 0 || H < 0 || Nq < 0 || (D != 64 && D != 128)) return QAT_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * H * Nq;
+  if (rows > kMaxRows) return QAT_ERR_INVALID_ARG;
+  if (rows == 0) return QAT_OK;
+  const void* ptrs[] = {o_q_acc, o_hp_acc, lse_acc, o_q_part, o_hp_part, lse_part};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return QAT_ERR_INVALID_ARG;
+  if ((o_q_out != nullptr && !aligned16(o_q_out)) || (o_hp_out != nullptr && !aligned16(o_hp_out)))
+    return QAT_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int num_sms = 0;
+  cudaError_t e = qat::device_context(&err, &num_sms);
+  if (e == cudaSuccess)
+    e = qat::launch_merge(o_q_acc, o_hp_acc, lse_acc, o_q_part, o_hp_part, lse_part,
+                          static_cast<uint16_t*>(o_q_out), static_cast<uint16_t*>(o_hp_out), rows,
+                          D, num_sms, static_cast<cudaStream_t>(stream));
   return from_cuda(e);
 }
 

@@ -29,7 +29,8 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int D) {
 
 // [BH, N, D] bf16 viewed as a 3-D TMA tensor (D innermost), 64 x 128 x 1 boxes,
 // 128-byte swizzle, zero fill out of bounds.
-bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH);
+bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH,
+                      int head_rows = -1);
 // [BH, N, D] fp32 as a 3-D TMA tensor with 32 x 16 x 1 boxes (128-byte rows, swizzled).
 bool make_f32_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH);
 
@@ -46,6 +47,9 @@ struct FwdArgs {
   float qk_scale;  // sm_scale * log2(e)
   int causal;
   int quant;
+  int kv_head_rows;  // rows between consecutive heads in K/V memory (Nkv unless a chunk)
+  float* o_q_f32;    // when set (with o_hp_f32), fp32 outputs replace the bf16 ones
+  float* o_hp_f32;
 };
 
 // Arguments of one backward launch.
@@ -75,6 +79,9 @@ cudaError_t launch_channel_mean(const uint16_t* x, float* mean, long long rows, 
                                 int num_sms, cudaStream_t s);
 cudaError_t launch_fake_quant_tokens(const uint16_t* x, const float* mean, uint16_t* out,
                                      float* scales, int BH, int N, int D, cudaStream_t s);
+cudaError_t launch_merge(float* o_q_acc, float* o_hp_acc, float* lse_acc, const float* o_q_part,
+                         const float* o_hp_part, const float* lse_part, uint16_t* o_q_out,
+                         uint16_t* o_hp_out, long long rows, int D, int num_sms, cudaStream_t s);
 cudaError_t launch_debug_quant(const float* p, int rows, int cols, float* deq,
                                float* scales, uint8_t* codes, cudaStream_t s);
 

@@ -105,3 +105,15 @@ def test_debug_quant_validation():
     assert capi.qat_debug_quant_tiles(None, -1, 4, A, A, A, stream=0) == Status.INVALID_ARG
     assert capi.qat_debug_quant_tiles(None, 4, 64, A, A, A, stream=0) == Status.INVALID_ARG
     assert capi.qat_debug_quant_tiles(None, 0, 64, None, None, None, stream=0) == Status.OK
+
+
+def test_chunk_and_merge_validation():
+    base = dict(q=A, k=A, v=A, o_q=A, o_hp=A, lse=A, B=1, H=1, Nq=8, Nkv_total=256, D=128,
+                sm_scale=0.1, quant_mode=1, stream=0)
+    assert capi.qat_attn_fwd_chunk(kv_begin=32, kv_len=64, **base) == Status.UNSUPPORTED
+    assert capi.qat_attn_fwd_chunk(kv_begin=192, kv_len=128, **base) == Status.INVALID_ARG
+    assert capi.qat_attn_fwd_chunk(kv_begin=-64, kv_len=64, **base) == Status.INVALID_ARG
+    assert capi.qat_attn_fwd_chunk(kv_begin=0, kv_len=0, **base) == Status.INVALID_ARG
+    assert capi.qat_attn_merge(A, A, None, A, A, A, None, None, 1, 1, 8, 128, 0) == Status.INVALID_ARG
+    assert capi.qat_attn_merge(A, A, A, A, A, A, None, None, 1, 1, 8, 96, 0) == Status.INVALID_ARG
+    assert capi.qat_attn_merge(None, None, None, None, None, None, None, None, 0, 1, 8, 128, 0) == Status.OK
