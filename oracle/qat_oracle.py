@@ -396,3 +396,25 @@ def merge_partials(o_a, lse_a, o_b, lse_b):
     tot = wa + wb
     o = (wa[..., None] * np.asarray(o_a, np.float64) + wb[..., None] * np.asarray(o_b, np.float64))
     return o / tot[..., None], lse
+
+
+# ---------------------------------------------------------------------------
+# The page's own backward variant (quant_mode 2)
+# ---------------------------------------------------------------------------
+# "attn_qat_train.py", _attn_bwd_dkdv: dv += dot(trans(p_quant), do) with
+# p_quant = fake_quantize(p) (the same per query row x KV tile quantization as the
+# forward), while ds = p * (dp - Di) uses the unquantized p; _attention.forward passes
+# o_for_bwd = O (the quantized output) to _attn_bwd_preprocess when use_high_prec_o is
+# False (its default), so Delta = rowsum(dO * O_q).
+
+def head_backward_page(q, k, v, do, sm_scale: float, causal: bool):
+    """dQ, dK, dV of the page's default backward for one head (fp64)."""
+    do = np.asarray(do, np.float64)
+    f = head_forward(q, k, v, sm_scale, causal, quant=True, return_p=True)
+    p, pq, o_q = f["p"], f["pq"], f["o_q"]
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    q = np.asarray(q, np.float64)
+    delta = (do * o_q).sum(axis=1)
+    ds = p * (do @ v.T - delta[:, None])
+    return sm_scale * (ds @ k), sm_scale * (ds.T @ q), pq.T @ do

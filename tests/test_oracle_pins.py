@@ -406,3 +406,29 @@ def test_chunk_not_aligned_to_quant_tiles_differs():
     oq, _ = orc.merge_partials(a[0], a[2], b[0], b[2])
     assert np.allclose(oh, full[1], rtol=1e-12)
     assert not np.allclose(oq, full[0], rtol=1e-9)
+
+
+# ---------------------------------------------------------------- the page's backward variant
+
+def test_page_backward_terms():
+    """dV uses the quantized P, Delta the quantized output, dS the unquantized P: checked
+    term by term against direct products of the oracle's own P, Pq and O_q, and against
+    the straight-through gradients where quantization leaves P unchanged."""
+    n, d = 90, 8
+    q, k, v, do = (rng_f64(70 + i, n, d) for i in range(4))
+    sc = 0.5
+    dq, dk, dv = orc.head_backward_page(q, k, v, do, sc, False)
+    f = orc.head_forward(q, k, v, sc, False, quant=True, return_p=True)
+    assert np.allclose(dv, f["pq"].T @ do, rtol=1e-12)
+    delta = (do * f["o_q"]).sum(axis=1)
+    ds = f["p"] * (do @ v.T - delta[:, None])
+    assert np.allclose(dk, sc * ds.T @ q, rtol=1e-12) and np.allclose(dq, sc * ds @ k, rtol=1e-12)
+    _, _, dv_ste = orc.head_backward(q, k, v, do, sc, False)
+    assert not np.allclose(dv, dv_ste, rtol=1e-6)          # the variants differ ...
+    assert rel_l2(dv, dv_ste) < 0.05                         # ... by the FP8 error only
+    # identical keys: every code is 448, Pq = P, so both variants agree exactly
+    kk = np.tile(rng_f64(75, 1, d), (n, 1))
+    a = orc.head_backward_page(q, kk, v, do, sc, False)
+    b = orc.head_backward(q, kk, v, do, sc, False)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-10, atol=1e-12)
