@@ -55,8 +55,14 @@ typedef enum {
 
 /* quant_mode values */
 enum {
-  QAT_QUANT_NONE = 0,                /* O_q is computed with P unquantized (= O_hp) */
-  QAT_QUANT_P_FP8E4M3_ROW_TILE64 = 1 /* P fake-quantized per row x 64-key tile      */
+  QAT_QUANT_NONE = 0,                 /* O_q is computed with P unquantized (= O_hp)  */
+  QAT_QUANT_P_FP8E4M3_ROW_TILE64 = 1, /* P fake-quantized per row x 64-key tile;
+                                         straight-through backward                     */
+  QAT_QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD = 2 /* forward as mode 1; the page's default
+                                         backward ("attn_qat_train.py", _attn_bwd_dkdv,
+                                         use_high_prec_o = False): dV from the quantized
+                                         P, Delta from O_q (pass O_q as `o_hp`), dS from
+                                         the unquantized P                               */
 };
 
 /*
@@ -109,7 +115,9 @@ QAT_API size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D
  *   Delta_i = sum_d dO_id O_hp,id;  P_ij = exp2(s_ij log2(e) - lse_i);
  *   dP = dO V^T;  dS = P o (dP - Delta);  dQ = sm_scale dS K;  dK = sm_scale dS^T Q;
  *   dV = P^T dO.
- *   quant_mode is validated but does not change the result (straight-through).
+ *   quant_mode 0 and 1: the straight-through estimator, as above.  quant_mode 2: the
+ *   page's default backward instead: pass the forward's O_q as `o_hp` (Delta =
+ *   rowsum(dO o O_q)) and dV = quant(P)^T dO with the forward's per-tile rule.
  *   workspace  device buffer of at least qat_attn_bwd_workspace_bytes(...) bytes,
  *              256-byte aligned, owned by the caller; its contents on entry are
  *              ignored and on exit unspecified.

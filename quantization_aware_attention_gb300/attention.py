@@ -116,7 +116,9 @@ class QATAttention(torch.autograd.Function):
         elif smooth_k:
             raise ValueError("smooth_k changes the result only together with qkv_quant")
         o_q, o_hp, lse = qat_attention_forward(q, k, v, causal, sm_scale, quant_mode)
-        ctx.save_for_backward(q, k, v, o_hp, lse)
+        # the page's backward variant forms Delta from O_q, the straight-through one from O_hp
+        o_bwd = o_q if quant_mode == capi.QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD else o_hp
+        ctx.save_for_backward(q, k, v, o_bwd, lse)
         ctx.causal, ctx.sm_scale, ctx.quant_mode = causal, sm_scale, quant_mode
         return o_q
 

@@ -43,6 +43,7 @@ class Status(enum.IntEnum):
 
 QUANT_NONE = 0
 QUANT_P_FP8E4M3_ROW_TILE64 = 1
+QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD = 2
 
 
 class QatError(RuntimeError):

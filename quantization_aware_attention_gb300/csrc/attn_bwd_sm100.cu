@@ -34,6 +34,7 @@
 //               accumulator), and per item one of dV / dK -> bf16 global.
 // TMEM (512 columns): S^T [0,128), dP^T / dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
 #include "qat_internal.h"
+#include "qat_quant.cuh"
 #include "sm100.cuh"
 
 #include <cuda.h>
@@ -61,7 +62,8 @@ struct BwdTc {
   static constexpr uint32_t kOffStage = kOffDS + 2 * kChunkBytes;  // dQ staging, 8 x 2 KB
   static constexpr uint32_t kOffLse = kOffStage + 16384;         // 2 stages x 512 B
   static constexpr uint32_t kOffDelta = kOffLse + 1024;          // 2 stages x 512 B
-  static constexpr uint32_t kOffBar = kOffDelta + 1024;
+  static constexpr uint32_t kOffPx = kOffDelta + 1024;   // quant_mode 2: tile maxima, scales
+  static constexpr uint32_t kOffBar = kOffPx + 8192;
   static constexpr uint32_t kOffMisc = kOffBar + 256;
   static constexpr uint32_t kUsed = kOffMisc + 64;
   static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
@@ -71,7 +73,7 @@ struct BwdTc {
 enum : uint32_t {
   B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL,
   B_DO_EMPTY, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL, B_DS_EMPTY, B_DQ_FULL, B_DQ_EMPTY,
-  B_DKDV_FULL, B_DKDV_EMPTY, B_DRAIN, B_COUNT
+  B_DKDV_FULL, B_DKDV_EMPTY, B_DRAIN, B_PX0, B_PX1, B_PX2, B_PX3, B_COUNT
 };
 
 struct BwdTcParams {
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (uint32_t i = 0; i < B_COUNT; ++i) {
       const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DQ_EMPTY ||
-                            i == B_DKDV_EMPTY) ? 256u : 1u;
+                            i == B_DKDV_EMPTY) ? 256u : (i >= B_PX0 ? 64u : 1u);
       mbar_init(bar(i), cnt);
     }
     fence_barrier_init();
@@ -354,6 +356,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(B_P_FULL));
       return true;
     };
+    // quant_mode 2 (the page's backward, "attn_qat_train.py" _attn_bwd_dkdv): the dV MMA
+    // consumes P^T quantized per (query, 64-key tile) with the forward's rule.  The 64
+    // keys of a tile are the lanes of a warp pair (quarters 0-1 or 2-3 of this group):
+    // column maxima by redux within each warp, exchanged through shared memory.
+    float* px = reinterpret_cast<float*>(gbase + C::kOffPx);          // [4][2 parity][2][64]
+    float* psc = reinterpret_cast<float*>(gbase + C::kOffPx + 4096);  // [8 warps][128]
+    const int pair = 2 * h + (quarter >> 1);
+    const int wip = quarter & 1;
+    auto p_phase_page = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
+      const uint32_t st = c & 1;
+      const float* sl = reinterpret_cast<const float*>(gbase + C::kOffLse + st * 512) + 64 * h;
+      if (!(wwait(bar(B_Q_FULL0 + st), (c >> 1) & 1) && wwait(bar(B_S_FULL), c & 1))) return false;
+      tc_fence_after();
+      const bool diag = p.a.causal && blk == kb;
+      const int qh = blk * kBlk + 64 * h;
+      uint32_t pf[64];                                 // P^T of this row, fp32 bits
+      tmem_ld32(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
+      tmem_ld32(tbase + lrow + C::kTmemS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 64; i += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pv = ex2f(fmaf(__uint_as_float(pf[i + e]), qk, -lv[e]));
+          if (!key_ok || (diag && qh + i + e < key)) pv = 0.f;
+          pf[i + e] = __float_as_uint(pv);
+        }
+        Pp[i / 2] = pack_bf16x2(__uint_as_float(pf[i]), __uint_as_float(pf[i + 1]));
+        Pp[i / 2 + 1] = pack_bf16x2(__uint_as_float(pf[i + 2]), __uint_as_float(pf[i + 3]));
+      }
+      // column maxima over this warp's 32 keys (non-negative floats order as their bits)
+      uint32_t mine0 = 0u, mine1 = 0u;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, pf[i]);
+        if ((i & 31) == lane) {
+          if (i < 32) mine0 = mx; else mine1 = mx;
+        }
+      }
+      float* slot = px + ((pair * 2 + (c & 1)) * 2) * 64;
+      slot[wip * 64 + lane] = __uint_as_float(mine0);
+      slot[wip * 64 + 32 + lane] = __uint_as_float(mine1);
+      mbar_arrive(bar(B_PX0 + pair));
+      if (!wwait(bar(B_PX0 + pair), c & 1)) return false;
+      const float a0 = fmaxf(__uint_as_float(mine0), slot[(wip ^ 1) * 64 + lane]);
+      const float a1 = fmaxf(__uint_as_float(mine1), slot[(wip ^ 1) * 64 + 32 + lane]);
+      const TileScale t0 = tile_scale(a0), t1 = tile_scale(a1);
+      float* ws = psc + (warp - 2) * 128;              // inv [0,64), scale [64,128)
+      ws[lane] = t0.inv;
+      ws[32 + lane] = t1.inv;
+      ws[64 + lane] = t0.scale;
+      ws[96 + lane] = t1.scale;
+      __syncwarp();
+      uint32_t pq[32];
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float2 inv = *reinterpret_cast<const float2*>(ws + i);
+        const float2 scl = *reinterpret_cast<const float2*>(ws + 64 + i);
+        const float2 x = mul_rn_f32x2(make_float2(__uint_as_float(pf[i]), __uint_as_float(pf[i + 1])), inv);
+        const float2 d = mul_rn_f32x2(e4m3x2_decode(e4m3x2_rn_satfinite(x.x, x.y)), scl);
+        pq[i / 2] = pack_bf16x2(d.x, d.y);
+      }
+      __syncwarp();                                    // ws is rewritten next block
+      tmem_st16(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<const uint32_t(*)[16]>(&pq[0]));
+      tmem_st16(tbase + lrow + C::kTmemS + 64 * h + 16,
+                *reinterpret_cast<const uint32_t(*)[16]>(&pq[16]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_FULL));
+      return true;
+    };
     // dS phase of block c: dS^T = P^T o (dP^T - Delta) -> bf16 into the dS^T smem tile
     auto ds_phase = [&](uint32_t c) -> bool {
       const float* sd =
@@ -448,11 +523,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool key_ok = key < p.a.Nkv;
       // order per block b: dS_b, P_{b+1}, drain_b -- the next block's P is ready for its
       // dV MMA before dQ_b has finished, and the reduce-add leaves the critical path
-      ok = p_phase(qc, block_at(first, 0, p), kb, key_ok, key);
+      auto pp = [&](uint32_t c_, int blk_) {
+        return p.a.page_bwd ? p_phase_page(c_, blk_, kb, key_ok, key)
+                            : p_phase(c_, blk_, kb, key_ok, key);
+      };
+      ok = pp(qc, block_at(first, 0, p));
       for (int ii = 0; ii < count && ok; ++ii, ++qc) {
         const int blk = block_at(first, ii, p);
         ok = ds_phase(qc);
-        if (ok && ii + 1 < count) ok = p_phase(qc + 1, block_at(first, ii + 1, p), kb, key_ok, key);
+        if (ok && ii + 1 < count) ok = pp(qc + 1, block_at(first, ii + 1, p));
         if (ok) ok = drain(qc, blk, bh);
       }
       if (!ok) break;

@@ -74,7 +74,8 @@ qat_status_t check_sizes(int B, int H, int Nq, int Nkv, int D, float sm_scale, i
   if (D != 64 && D != 128) return QAT_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !isfinite(sm_scale)) return QAT_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return QAT_ERR_INVALID_ARG;
-  if (quant_mode != QAT_QUANT_NONE && quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64)
+  if (quant_mode != QAT_QUANT_NONE && quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64 &&
+      quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD)
     return QAT_ERR_INVALID_ARG;
   if (B == 0 || H == 0) {
     *empty = true;
@@ -136,7 +137,7 @@ qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v, void* o_q
   a.sm_scale = sm_scale;
   a.qk_scale = sm_scale * kLog2e;
   a.causal = causal;
-  a.quant = quant_mode == QAT_QUANT_P_FP8E4M3_ROW_TILE64;
+  a.quant = quant_mode != QAT_QUANT_NONE;
   a.kv_head_rows = Nkv;
   a.o_q_f32 = nullptr;
   a.o_hp_f32 = nullptr;
@@ -172,7 +173,7 @@ qat_status_t qat_attn_fwd_chunk(const void* q, const void* k, const void* v, flo
   a.sm_scale = sm_scale;
   a.qk_scale = sm_scale * kLog2e;
   a.causal = 0;
-  a.quant = quant_mode == QAT_QUANT_P_FP8E4M3_ROW_TILE64;
+  a.quant = quant_mode != QAT_QUANT_NONE;
   a.kv_head_rows = Nkv_total;
   a.o_q_f32 = o_q;
   a.o_hp_f32 = o_hp;
@@ -256,6 +257,7 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.sm_scale = sm_scale;
   a.qk_scale = sm_scale * kLog2e;
   a.causal = causal;
+  a.page_bwd = quant_mode == QAT_QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD;
   unsigned int* err = nullptr;
   int num_sms = 0;
   cudaError_t e = qat::device_context(&err, &num_sms);

@@ -70,6 +70,7 @@ struct BwdArgs {
   float sm_scale;
   float qk_scale;
   int causal;
+  int page_bwd;     // 1: dV from quantized P and Delta from the O passed (O_q)
 };
 
 // Kernel launchers (return cudaGetLastError() after the launches).

@@ -65,6 +65,7 @@ def bwd(**kw):
     (dict(sm_scale=float("inf")), Status.INVALID_ARG),
     (dict(causal=2), Status.INVALID_ARG),
     (dict(quant_mode=7), Status.INVALID_ARG),
+    (dict(quant_mode=3), Status.INVALID_ARG),
     (dict(q=None), Status.INVALID_ARG),
     (dict(lse=None), Status.INVALID_ARG),
     (dict(o_hp=A + 8), Status.INVALID_ARG),
