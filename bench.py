@@ -325,40 +325,72 @@ def run_ours(args, w):
     ms_step = total_ms / args.steps
     value = whole_job_tflops(flops_step, args.steps, world, total_ms)
 
-    # ---- end to end: host buffers, copies inside the timed region
+    # ---- end to end: host buffers, every step's copies inside the timed region.  Steps
+    # are pipelined over two device buffer sets: the host-to-device copy of step i + 1 and
+    # the device-to-host read of step i - 1 run on their own streams while step i computes.
     hout = {}
     if not args.no_e2e:
         hout = {n: torch.empty(host["q"].shape, dtype=torch.bfloat16).pin_memory()
                 for n in ("o_q", "dq")}
         hout.update({n: torch.empty(host["k"].shape, dtype=torch.bfloat16).pin_memory()
                      for n in ("dk", "dv")})
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) if hout else 0
     d2h = sum(t.numel() * t.element_size() for t in hout.values())
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 10))
+    e2e_ms = 0.0
+    if e2e_steps:
+        xs = [x, {n: torch.empty_like(t) for n, t in x.items()}]
+        outs = [dict(o_q=o_q, o_hp=o_hp, lse=lse, dq=dq, dk=dk, dv=dv)]
+        outs.append({n: torch.empty_like(t) for n, t in outs[0].items()})
+        s_in = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_cmp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for n, t in host.items():
-            x[n].copy_(t, non_blocking=True)
-        fwd()
-        bwd()
-        hout["o_q"].copy_(o_q, non_blocking=True)
-        hout["dq"].copy_(dq, non_blocking=True)
-        hout["dk"].copy_(dk, non_blocking=True)
-        hout["dv"].copy_(dv, non_blocking=True)
+        def run_e2e(n_steps):
+            for i in range(n_steps):
+                b = i & 1
+                xb, ob = xs[b], outs[b]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(ev_cmp[b])        # step i - 2 is done with xb
+                    for n, t in host.items():
+                        xb[n].copy_(t, non_blocking=True)
+                    ev_in[b].record(s_in)
+                stream.wait_event(ev_in[b])
+                if i >= 2:
+                    stream.wait_event(ev_out[b])          # ob has been read back
+                for name, st in (("qat_attn_fwd", capi.qat_attn_fwd(
+                        xb["q"], xb["k"], xb["v"], ob["o_q"], ob["o_hp"], ob["lse"], B, H, Nq,
+                        Nkv, D, sm, int(w.causal), capi.QUANT_P_FP8E4M3_ROW_TILE64, stream)),
+                                 ("qat_attn_bwd", capi.qat_attn_bwd(
+                        xb["q"], xb["k"], xb["v"], ob["o_hp"], ob["lse"], xb["do"], ob["dq"],
+                        ob["dk"], ob["dv"], B, H, Nq, Nkv, D, sm, int(w.causal),
+                        capi.QUANT_P_FP8E4M3_ROW_TILE64, ws, ws_bytes, stream))):
+                    if st != capi.Status.OK:
+                        raise capi.QatError(st, name)
+                ev_cmp[b].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_cmp[b])
+                    for n in ("o_q", "dq", "dk", "dv"):
+                        hout[n].copy_(ob[n], non_blocking=True)
+                    ev_out[b].record(s_out)
+            stream.wait_event(ev_out[(n_steps - 1) & 1])
+            if n_steps >= 2:
+                stream.wait_event(ev_out[(n_steps - 2) & 1])
 
-    if args.no_e2e:
-        e2e_steps = 0
-    else:
-        e2e_step()
-    barrier()
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    s1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
+        run_e2e(2)
+        barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        s_in.wait_event(s0)
+        run_e2e(e2e_steps)
+        s1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
+        del xs[1], outs[1]
     e2e_value = whole_job_tflops(flops_step, e2e_steps, world, e2e_ms) if e2e_steps else None
 
     # ---- the Q/K/V fake-quantization row (HBM-bound): channel mean of K + 3 passes
@@ -458,7 +490,10 @@ def run_ours(args, w):
             "algorithmic_flops_per_launch": 10.0 * pairs * D,
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "how": "pinned-host inputs copied in and O_q, dQ, dK, dV copied out every "
+                       "step through the C ABI; copies on their own streams overlap the "
+                       "neighbouring steps' compute (two device buffer sets)"},
         "gpu_launches": launches_per_step * args.steps,
         "next_rows": {
             "qkv_fake_quant": dict(qkv, frac_of_hbm=qkv["gbs"] / float(
