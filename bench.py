@@ -68,17 +68,21 @@ def whole_job_tflops(flops_per_step_per_rank: float, steps: int, world: int,
     return world * flops_per_step_per_rank * steps / (max_ms * 1e-3) / 1e12
 
 
-def kernel_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` at the benchmarked workload, from the committed
-    ncu summary, or None when the kernel's source has changed since the capture."""
+def kernel_traffic(*kernels: str):
+    """DRAM bytes per launch of `kernels` together at the benchmarked workload, from the
+    committed ncu summary, or None when any kernel's source has changed since the capture."""
     import hashlib
+    total = 0
     try:
         with open(os.path.join(ROOT, "profiles", "roofline_traffic.json")) as f:
-            rec = json.load(f)[kernel]
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
-                return None
-        return rec["dram_bytes_per_launch"]
+            recs = json.load(f)
+        for kernel in kernels:
+            rec = recs[kernel]
+            with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                    return None
+            total += rec["dram_bytes_per_launch"]
+        return total
     except (OSError, KeyError, ValueError):
         return None
 
@@ -273,7 +277,7 @@ def run_ours(args, w):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sm = w.sm_scale
-    launches_per_step = 4  # fwd kernel; bwd prep, tcgen05 main, dQ convert kernels
+    launches_per_step = 4  # fwd kernel; bwd prep, dK/dV and dQ kernels
 
     def fwd():
         st = capi.qat_attn_fwd(x["q"], x["k"], x["v"], o_q, o_hp, lse, B, H, Nq, Nkv, D, sm,
@@ -481,11 +485,12 @@ def run_ours(args, w):
         "tflops_flash_convention": world * 14.0 * pairs * D * args.steps / (total_ms * 1e-3) / 1e12,
         "tokens_per_s": world * B * Nq * args.steps / (total_ms * 1e-3),
         "roofline": {
-            "kernel": "qat_attn_bwd call (prep + attn_bwd_tc_kernel + dQ convert)",
+            "kernel": "qat_attn_bwd call (prep + attn_bwd_dkdv_kernel + attn_bwd_dq_kernel)",
             "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
             "frac": bwd_tf / peak_sus,
-            "traffic": kernel_traffic("attn_bwd_tc_kernel") if w.name == WORKLOAD else None,
-            "traffic_unit": "bytes per launch of attn_bwd_tc_kernel (DRAM read + write)",
+            "traffic": (kernel_traffic("attn_bwd_dkdv_kernel", "attn_bwd_dq_kernel")
+                        if w.name == WORKLOAD else None),
+            "traffic_unit": "bytes per qat_attn_bwd call: its dK/dV and dQ kernels (DRAM read + write)",
             "peak_kind": f"bf16_tflops_sustained ({peak_src})",
             "algorithmic_flops_per_launch": 10.0 * pairs * D,
         },

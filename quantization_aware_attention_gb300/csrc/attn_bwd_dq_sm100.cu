@@ -1,0 +1,442 @@
+// attn_bwd_dq_sm100.cu -- dQ of the QAT attention backward on the Blackwell tensor core
+// (tcgen05 + TMEM + TMA), warp-specialized and persistent.  One CTA owns a 128-row query
+// block and walks the key blocks, so dQ is summed in TMEM and written once: no atomics,
+// and the result does not depend on the order the CTAs run in.
+//
+// Per query row i and key block j ("attn_qat_train.py", _attn_bwd_dq; P rematerialized
+// from the saved base-2 lse):
+//   S = Q K_j^T,  P = exp2(S qk_scale - lse_i),  dP = dO V_j^T,
+//   dS = P o (dP - Delta_i),  dQ += dS K_j       (dQ scaled by sm_scale at the end)
+// P is the unquantized probability in every quant mode: the straight-through estimator
+// passes the gradient of O_q through the quantizer as the identity.
+//
+// CTA layout (352 threads, one CTA per SM, persistent over (head, 128-row query block)):
+//   warp 0      TMA producer: K_j (3-stage ring) and V_j (3-stage ring), 128 keys x D.
+//   warps 1, 2  MMA issuers (lane 0 of each), all MMAs with A in TMEM:
+//                 warp 1:  S  = Q K_j^T   (A = Q bf16 in TMEM, B = K_j K-major)  -> TMEM S
+//                 warp 2:  dQ += dS K_j   (A = dS bf16 in TMEM, B = K_j MN-major), then
+//                          dP = dO V_{j+1}^T (A = dO bf16 in TMEM, B = V K-major) -> dP
+//               One thread issues at most one MMA per ~93 cycles on this GPU, well under
+//               the tensor core's rate for M = 128, N = 128; two issuing warps keep it
+//               busy.  Each stream is ordered on its own; dP_{j+1} overwrites the dS_j
+//               that dQ_j reads, so both sit in warp 2's stream.  Warp 1 also owns TMEM.
+//   warps 3-10  two compute warpgroups; group h owns keys [64h, 64h + 64) of every
+//               block, each thread one query row (TMEM lane).  Per item they copy the
+//               Q rows (h = 0) or dO rows (h = 1) into TMEM, and at the end store their
+//               half of dQ's columns.  dS is written over the group's own dP columns.
+// Only the MMAs read shared memory (the B operands), which keeps the shared-memory
+// traffic per block at a fraction of an all-SS design.
+// TMEM (512 columns): S [0,128), dP / dS [128,256), dQ [256,256+D), Q [256+D, 256+3D/2),
+// dO [256+3D/2, 256+2D).
+#include "qat_internal.h"
+#include "qat_quant.cuh"
+#include "sm100.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+namespace qat {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBlk = 128;       // queries per item, keys per block
+constexpr int kThreads = 352;
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+
+template <int D>
+struct BwdDq {
+  static constexpr int kChunks = D / 64;
+  static constexpr uint32_t kChunkBytes = kBlk * 128;      // 16 KB box: 128 rows x 128 B
+  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr uint32_t kOffMisc = kOffBar + 256;
+  static constexpr uint32_t kUsed = kOffMisc + 64;
+  // at least 116 KB so that no two CTAs share an SM (each holds all 512 TMEM columns)
+  static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
+  static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
+  static constexpr uint32_t kTmemQ = 256 + D, kTmemDO = 256 + D + D / 2;
+};
+
+enum : uint32_t {
+  Q_K_FULL = 0, Q_K_EMPTY = Q_K_FULL + kKStages, Q_V_FULL = Q_K_EMPTY + kKStages,
+  Q_V_EMPTY = Q_V_FULL + kVStages, Q_S_FULL = Q_V_EMPTY + kVStages, Q_S_EMPTY, Q_DP_FULL,
+  Q_DS_FULL, Q_QD_FULL, Q_QD_EMPTY, Q_DQ_FULL, Q_DQ_EMPTY, Q_DRAIN_A, Q_DRAIN_B, Q_COUNT
+};
+
+struct DqParams {
+  BwdArgs a;
+  unsigned int* err;
+  int mtiles;   // query blocks per head
+  int ntiles;   // key blocks per head
+  int items;    // B * H * mtiles
+  int nq_pad;   // mtiles * 128
+};
+
+__device__ __forceinline__ void dq_item(int idx, const DqParams& p, int& bh, int& mt, int& J) {
+  const int BH = p.a.B * p.a.H;
+  if (p.a.causal) {  // longest first: late query blocks see the most keys
+    mt = p.mtiles - 1 - idx / BH;
+    bh = idx % BH;
+    J = min(p.ntiles, mt + 1);
+  } else {           // head-major: the CTAs running together share one head's K/V in L2
+    bh = idx / p.mtiles;
+    mt = idx % p.mtiles;
+    J = p.ntiles;
+  }
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const DqParams p) {
+  using C = BwdDq<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 8);
+  const uint32_t bars = base + C::kOffBar;
+  auto bar = [&](uint32_t i) { return bars + 8u * i; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (uint32_t i = 0; i < Q_COUNT; ++i) {
+      const bool wg = i == Q_S_EMPTY || i == Q_DS_FULL || i == Q_QD_FULL || i == Q_DQ_EMPTY;
+      // K tiles and the item's Q / dO rows are read by both issuers: one commit from each
+      const bool both = (i >= Q_K_EMPTY && i < Q_K_EMPTY + kKStages) || i == Q_QD_EMPTY;
+      mbar_init(bar(i), wg ? 256u : (both ? 2u : 1u));
+    }
+    fence_barrier_init();
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kc = 0, vc = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x) {
+        int bh, mt, J;
+        dq_item(idx, p, bh, mt, J);
+        for (int j = 0; j < J && ok; ++j) {
+          {
+            const uint32_t st = kc % kKStages, use = kc / kKStages;
+            ok = mbar_wait(bar(Q_K_EMPTY + st), (use & 1) ^ 1, abort_flag, p.err);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(Q_K_FULL + st), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(base + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes, &tmK,
+                          bar(Q_K_FULL + st), 64 * c, j * kBlk, bh);
+            ++kc;
+          }
+          {
+            const uint32_t st = vc % kVStages, use = vc / kVStages;
+            ok = mbar_wait(bar(Q_V_EMPTY + st), (use & 1) ^ 1, abort_flag, p.err);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(Q_V_FULL + st), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(base + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes, &tmV,
+                          bar(Q_V_FULL + st), 64 * c, j * kBlk, bh);
+            ++vc;
+          }
+        }
+      }
+      // drain: every issued load lands before the CTA exits
+      for (uint32_t i = (kc > kKStages ? kc - kKStages : 0); i < kc; ++i)
+        mbar_wait(bar(Q_K_FULL + i % kKStages), (i / kKStages) & 1, abort_flag, p.err);
+      for (uint32_t i = (vc > kVStages ? vc - kVStages : 0); i < vc; ++i)
+        mbar_wait(bar(Q_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer A: S
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kBlk, kBlk, false);
+      uint32_t kc = 0, bc = 0;  // K tiles, blocks (global counts)
+      int it = 0;
+      bool ok = true, issued = false;
+      auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, mt, J;
+        dq_item(idx, p, bh, mt, J);
+        ok = w(bar(Q_QD_FULL), it & 1);  // this item's Q and dO rows are in TMEM
+        for (int j = 0; j < J && ok; ++j, ++kc, ++bc) {
+          // S_j overwrites S_{j-1}: wait until the compute warps have read it
+          if (bc > 0 && !(ok = w(bar(Q_S_EMPTY), (bc - 1) & 1))) break;
+          const uint32_t st = kc % kKStages;
+          if (!(ok = w(bar(Q_K_FULL + st), (kc / kKStages) & 1))) break;
+          tc_fence_after();
+          const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+            mma_ts(tbase + C::kTmemS, tbase + C::kTmemQ + 8 * ks,
+                   smem_desc_sw128(sk + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(bar(Q_S_FULL));
+          mma_commit(bar(Q_K_EMPTY + st));
+          if (j + 1 == J) mma_commit(bar(Q_QD_EMPTY));  // the item's last read of Q
+        }
+      }
+      if (issued) {
+        mma_commit(bar(Q_DRAIN_A));
+        mbar_wait(bar(Q_DRAIN_A), 0, abort_flag, p.err);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ MMA issuer B: dQ, dP
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kBlk, kBlk, false);  // dP
+      constexpr uint32_t idQ = idesc_bf16_f32(kBlk, D, true);      // dQ (B = K MN-major)
+      uint32_t kc = 0, vc = 0, bc = 0;  // K tiles, V tiles, blocks (global counts)
+      int it = 0;
+      bool ok = true, issued = false;
+      auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
+      // dP = dO V^T into TMEM dP (after the previous dQ in this stream, which read dS there)
+      auto issue_dp = [&](uint32_t v, bool last) -> bool {
+        const uint32_t st = v % kVStages;
+        if (!w(bar(Q_V_FULL + st), (v / kVStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t sv = base + C::kOffV + st * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          mma_ts(tbase + C::kTmemDP, tbase + C::kTmemDO + 8 * ks,
+                 smem_desc_sw128(sv + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+        }
+        issued = true;
+        mma_commit(bar(Q_V_EMPTY + st));
+        mma_commit(bar(Q_DP_FULL));
+        if (last) mma_commit(bar(Q_QD_EMPTY));  // the item's last read of dO
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, mt, J;
+        dq_item(idx, p, bh, mt, J);
+        ok = w(bar(Q_QD_FULL), it & 1) && issue_dp(vc, J == 1);
+        for (int j = 0; j < J && ok; ++j) {
+          // dQ += dS_j K_j: dS_j (keys [64g, 64g + 64) in group g's dP columns)
+          if (!(ok = w(bar(Q_DS_FULL), bc & 1))) break;
+          if (j == 0 && it > 0 && !(ok = w(bar(Q_DQ_EMPTY), (it - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t st = kc % kKStages;
+          const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kBlk / 16; ++ks)
+            mma_ts(tbase + C::kTmemDQ, tbase + C::kTmemDP + (ks < 4 ? 8 * ks : 32 + 8 * ks),
+                   smem_desc_sw128(sk + ks * 2048, C::kChunkBytes, 1024), idQ,
+                   (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(Q_K_EMPTY + st));
+          ++kc;
+          ++bc;
+          ++vc;
+          if (j + 1 < J) {
+            if (!(ok = issue_dp(vc, j + 2 == J))) break;
+          } else {
+            mma_commit(bar(Q_DQ_FULL));
+          }
+        }
+      }
+      if (issued) {
+        mma_commit(bar(Q_DRAIN_B));
+        mbar_wait(bar(Q_DRAIN_B), 0, abort_flag, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ compute warpgroups
+    const int h = (warp - 3) >> 2;
+    const int quarter = warp & 3;                    // TMEM lane quarter of this warp
+    const int r = 32 * quarter + lane;               // query row of the block (TMEM lane)
+    const uint32_t lrow = (32u * quarter) << 16;
+    const float qk = p.a.qk_scale;
+    auto wwait = [&](uint32_t b_, uint32_t par) {
+      const bool okw = mbar_wait(b_, par, abort_flag, p.err);
+      return __all_sync(0xffffffffu, okw) != 0;
+    };
+    // Q (h = 0) or dO (h = 1) row of this thread into TMEM as bf16 pairs; rows past Nq
+    // are zero (their lse is +inf, so P = 0 there)
+    auto load_rows = [&](int bh, int mt) {
+      const int row = mt * kBlk + r;
+      const uint16_t* src = (h ? p.a.dO : p.a.q) + (static_cast<size_t>(bh) * p.a.Nq + row) * D;
+      const uint32_t dst = tbase + lrow + (h ? C::kTmemDO : C::kTmemQ);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (row < p.a.Nq) x = *reinterpret_cast<const uint4*>(src + 64 * c + 8 * u);
+          v[4 * u] = x.x;
+          v[4 * u + 1] = x.y;
+          v[4 * u + 2] = x.z;
+          v[4 * u + 3] = x.w;
+        }
+        tmem_st32(dst + 32 * c, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(Q_QD_FULL));
+    };
+    uint32_t bc = 0;
+    int it = 0;
+    bool ok = true;
+    if (static_cast<int>(blockIdx.x) < p.items) {
+      int bh, mt, J;
+      dq_item(blockIdx.x, p, bh, mt, J);
+      load_rows(bh, mt);
+    }
+    for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+      int bh, mt, J;
+      dq_item(idx, p, bh, mt, J);
+      const int row = mt * kBlk + r;
+      const size_t prow = static_cast<size_t>(bh) * p.nq_pad + row;
+      const float lse_r = p.a.lse_pad[prow];
+      const float delta_r = p.a.delta[prow];
+      for (int j = 0; j < J && ok; ++j, ++bc) {
+        if (!(ok = wwait(bar(Q_S_FULL), bc & 1))) break;
+        tc_fence_after();
+        uint32_t pr[64];                               // S, then P, of this row's 64 keys
+        tmem_ld32(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+        tmem_ld32(tbase + lrow + C::kTmemS + 64 * h + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(Q_S_EMPTY));
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float2 x = fma_rn_f32x2(make_float2(__uint_as_float(pr[i]), __uint_as_float(pr[i + 1])),
+                                        make_float2(qk, qk), make_float2(-lse_r, -lse_r));
+          pr[i] = __float_as_uint(ex2f(x.x));
+          pr[i + 1] = __float_as_uint(ex2f(x.y));
+        }
+        // keys past Nkv, and keys after the row on the causal diagonal: P = 0 (a
+        // warp-uniform pass over the few blocks that have such keys)
+        const int key0 = j * kBlk + 64 * h;
+        if (key0 + 64 > p.a.Nkv || (p.a.causal && j == mt)) {
+          const int lim = p.a.causal ? min(p.a.Nkv - 1, row) : p.a.Nkv - 1;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (key0 + i > lim) pr[i] = 0u;
+        }
+        if (!(ok = wwait(bar(Q_DP_FULL), bc & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t dr[32];
+          tmem_ld32(tbase + lrow + C::kTmemDP + 64 * h + 32 * cc, dr);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 d = mul_rn_f32x2(
+                make_float2(__uint_as_float(pr[32 * cc + 2 * i]), __uint_as_float(pr[32 * cc + 2 * i + 1])),
+                add_rn_f32x2(make_float2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])),
+                             make_float2(-delta_r, -delta_r)));
+            pk[i] = pack_bf16x2(d.x, d.y);
+          }
+          // dS of keys [64h + 32cc, +32) over dP columns this thread has already read
+          tmem_st16(tbase + lrow + C::kTmemDP + 64 * h + 16 * cc, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(Q_DS_FULL));
+      }
+      if (!ok) break;
+      // the next item's Q / dO rows go in while this item's last dQ MMA runs
+      const int nidx = idx + static_cast<int>(gridDim.x);
+      if (nidx < p.items) {
+        if (!(ok = wwait(bar(Q_QD_EMPTY), it & 1))) break;
+        tc_fence_after();
+        int nbh, nmt, nJ;
+        dq_item(nidx, p, nbh, nmt, nJ);
+        load_rows(nbh, nmt);
+      }
+      // ---- epilogue: group h stores dQ columns [hD/2, (h+1)D/2) of its row
+      if (!(ok = wwait(bar(Q_DQ_FULL), it & 1))) break;
+      tc_fence_after();
+      uint32_t o[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(tbase + lrow + C::kTmemDQ + (D / 2) * h + 32 * c,
+                  *reinterpret_cast<uint32_t(*)[32]>(&o[32 * c]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(Q_DQ_EMPTY));
+      if (row < p.a.Nq) {
+        const float sc = p.a.sm_scale;
+        uint4* dst = reinterpret_cast<uint4*>(p.a.dq + (static_cast<size_t>(bh) * p.a.Nq + row) * D +
+                                              (D / 2) * h);
+#pragma unroll
+        for (int v = 0; v < D / 16; ++v)
+          dst[v] = make_uint4(
+              pack_bf16x2(__uint_as_float(o[8 * v]) * sc, __uint_as_float(o[8 * v + 1]) * sc),
+              pack_bf16x2(__uint_as_float(o[8 * v + 2]) * sc, __uint_as_float(o[8 * v + 3]) * sc),
+              pack_bf16x2(__uint_as_float(o[8 * v + 4]) * sc, __uint_as_float(o[8 * v + 5]) * sc),
+              pack_bf16x2(__uint_as_float(o[8 * v + 6]) * sc, __uint_as_float(o[8 * v + 7]) * sc));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int D>
+cudaError_t launch_bwd_dq_d(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
+  using C = BwdDq<D>;
+  const int BH = a.B * a.H;
+  DqParams p;
+  p.a = a;
+  p.err = err;
+  p.mtiles = (a.Nq + kBlk - 1) / kBlk;
+  p.ntiles = (a.Nkv + kBlk - 1) / kBlk;
+  p.items = BH * p.mtiles;
+  p.nq_pad = p.mtiles * kBlk;
+  CUtensorMap mk, mv;
+  if (!make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) || !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int grid = p.items < num_sms ? p.items : num_sms;
+  attn_bwd_dq_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
+  return a.D == 64 ? launch_bwd_dq_d<64>(a, err, num_sms, s)
+                   : launch_bwd_dq_d<128>(a, err, num_sms, s);
+}
+
+}  // namespace qat

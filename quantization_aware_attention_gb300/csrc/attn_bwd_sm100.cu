@@ -1,38 +1,43 @@
 // attn_bwd_sm100.cu -- QAT attention backward (straight-through estimator) on the
-// Blackwell tensor core (tcgen05 + TMEM + TMA), warp-specialized and persistent.
+// Blackwell tensor core (tcgen05 + TMEM + TMA): the preprocessing kernel and dK, dV.
+// dQ comes from its own kernel (attn_bwd_dq_sm100.cu), as in the page's split into a
+// dK/dV program and a dQ program.
 //
 // Gradients of L = <dO, O_hp> ("attn_qat_train.py", _attn_bwd_preprocess,
-// _attn_bwd_dkdv, _attn_bwd_dq; P rematerialized from the saved base-2 lse as
-// "support for pytorch autograd" suggests):
+// _attn_bwd_dkdv; P rematerialized from the saved base-2 lse as "support for pytorch
+// autograd" suggests):
 //   Delta_i = sum_d dO_id O_hp,id
 //   P^T = exp2(S^T qk_scale - lse)     S^T = K Q^T
 //   dP^T = V dO^T,   dS^T = P^T o (dP^T - Delta)
-//   dV += P^T dO,    dK += dS^T Q,    dQ += dS K     (dK, dQ scaled by sm_scale at the end)
+//   dV += P^T dO,    dK += dS^T Q     (dK scaled by sm_scale at the end)
 //
 // Kernels, in launch order on the caller's stream:
-//   bwd_prep_kernel     Delta and a copy of lse padded to 128-row blocks (+inf in the
-//                       padding, so P = 0 there), and zeroes the fp32 dQ accumulator.
-//   attn_bwd_tc_kernel  one CTA per SM, persistent over (head, 128-key block) items.
-//   dq_convert_kernel   dQ = bf16(dQ_acc * sm_scale).
+//   bwd_prep_kernel       Delta and a copy of lse padded to 128-row blocks (+inf in the
+//                         padding, so P = 0 there).
+//   attn_bwd_dkdv_kernel  one CTA per SM, persistent over (head, 128-key block) items.
+//   attn_bwd_dq_kernel    one CTA per SM, persistent over (head, 128-row query block).
 //
-// attn_bwd_tc_kernel, 320 threads:
-//   warp 0      TMA producer: K, V once per item; per 128-row query block Q (2-stage
-//               ring, with its lse and Delta rows by 1-D bulk copy) and dO (1 stage).
-//   warp 1      TMEM allocator; lane 0 issues all MMAs:
-//                 S^T  = K Q^T     SS  -> TMEM [0,128)      (A = K, B = Q, both K-major)
-//                 dP^T = V dO^T    SS  -> TMEM [128,256)
-//                 dV  += P^T dO    TS  (A = P^T bf16 in TMEM [0,32) + [64,96), B = dO MN-major)
-//                 dQ   = dS K      SS  -> TMEM [128,128+D)   (A = dS: the dS^T smem tile
-//                                       read MN-major; B = K MN-major)
-//                 dK  += dS^T Q    SS  (A = dS^T K-major, B = Q MN-major)
-//               steady-state order per block b: dV_b, S^T_{b+1}, dQ_b, dK_b, dP^T_{b+1},
-//               so the softmax warps and the dQ drain overlap tensor-core work.
-//   warps 2-9   two compute warpgroups, each owning 64 of a block's 128 query columns:
-//               P phase (P^T from S^T, bf16 into TMEM for dV), dS phase (dS^T from dP^T,
-//               bf16 into a 128-byte-swizzled smem tile), dQ drain (half of dQ's
-//               columns out of TMEM, then TMA bulk reduce-add into the fp32
-//               accumulator), and per item one of dV / dK -> bf16 global.
-// TMEM (512 columns): S^T [0,128), dP^T / dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
+// attn_bwd_dkdv_kernel, 352 threads:
+//   warp 0      TMA producer: K, V once per item; per 128-row query block Q and dO
+//               (2-stage rings; Q's stage also carries its lse and Delta rows by 1-D
+//               bulk copy).
+//   warps 1, 2  MMA issuers (lane 0 of each); warp 1 also owns TMEM:
+//                 warp 1:  dV  += P^T dO   TS  (A = P^T bf16 in TMEM [0,32) + [64,96),
+//                                               B = dO MN-major), then
+//                          S^T  = K Q^T    SS  -> TMEM [0,128)   (A = K, B = Q, K-major)
+//                 warp 2:  dK  += dS^T Q   TS  (A = dS^T bf16 in TMEM [128,160) +
+//                                               [192,224), B = Q MN-major), then
+//                          dP^T = V dO^T   SS  -> TMEM [128,256)
+//               One thread issues at most one MMA per ~93 cycles on this GPU, so two
+//               issuers keep the tensor core busy.  Each stream only overwrites TMEM that
+//               its own earlier MMAs read (S^T over P^T, dP^T over dS^T), so in-order
+//               issue within a stream is all the ordering the TMEM reuse needs; operands
+//               both streams read (Q, dO, K/V) are released by one commit from each.
+//   warps 3-10  two compute warpgroups, each owning 64 of a block's 128 query columns:
+//               P phase (P^T from S^T, bf16 over the group's S^T columns), dS phase
+//               (dS^T from dP^T, bf16 over the group's dP^T columns), and per item one of
+//               dV / dK -> bf16 global.
+// TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
 #include "qat_internal.h"
 #include "qat_quant.cuh"
 #include "sm100.cuh"
@@ -47,7 +52,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kBlk = 128;       // keys per item, queries per block
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 
 template <int D>
 struct BwdTc {
@@ -57,10 +62,8 @@ struct BwdTc {
   static constexpr uint32_t kOffK = 0;
   static constexpr uint32_t kOffV = kOffK + kTileBytes;
   static constexpr uint32_t kOffQ = kOffV + kTileBytes;     // 2 stages
-  static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;
-  static constexpr uint32_t kOffDS = kOffDO + kTileBytes;   // 128 x 128 bf16, 2 chunks
-  static constexpr uint32_t kOffStage = kOffDS + 2 * kChunkBytes;  // dQ staging, 8 x 2 KB
-  static constexpr uint32_t kOffLse = kOffStage + 16384;         // 2 stages x 512 B
+  static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;  // 2 stages
+  static constexpr uint32_t kOffLse = kOffDO + 2 * kTileBytes;   // 2 stages x 512 B
   static constexpr uint32_t kOffDelta = kOffLse + 1024;          // 2 stages x 512 B
   static constexpr uint32_t kOffPx = kOffDelta + 1024;   // quant_mode 2: tile maxima, scales
   static constexpr uint32_t kOffBar = kOffPx + 8192;
@@ -71,9 +74,9 @@ struct BwdTc {
 };
 
 enum : uint32_t {
-  B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL,
-  B_DO_EMPTY, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL, B_DS_EMPTY, B_DQ_FULL, B_DQ_EMPTY,
-  B_DKDV_FULL, B_DKDV_EMPTY, B_DRAIN, B_PX0, B_PX1, B_PX2, B_PX3, B_COUNT
+  B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL0,
+  B_DO_FULL1, B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL,
+  B_DKDV_FULL, B_DKDV_EMPTY, B_DRAIN, B_DRAIN_B, B_PX0, B_PX1, B_PX2, B_PX3, B_COUNT
 };
 
 struct BwdTcParams {
@@ -93,8 +96,8 @@ __device__ __forceinline__ void bwd_item(int idx, const BwdTcParams& p, int& bh,
     bh = idx % BH;
     first = kb;
     count = p.mtiles - kb;
-  } else {           // head-major; each item starts at a different query block so that
-    bh = idx / p.ktiles;  // the CTAs of one head spread their dQ atomics
+  } else {           // head-major: the CTAs running together share one head's Q/dO in L2
+    bh = idx / p.ktiles;
     kb = idx % p.ktiles;
     first = kb % p.mtiles;
     count = p.mtiles;
@@ -120,11 +123,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                       const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdTcParams p) {
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmDO, const BwdTcParams p) {
   using C = BwdTc<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -139,8 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     *abort_flag = 0;
     for (uint32_t i = 0; i < B_COUNT; ++i) {
-      const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DQ_EMPTY ||
-                            i == B_DKDV_EMPTY) ? 256u : (i >= B_PX0 ? 64u : 1u);
+      // released by one commit from each MMA issuer
+      const bool both = i == B_KV_EMPTY || i == B_Q_EMPTY0 || i == B_Q_EMPTY1 ||
+                        i == B_DO_EMPTY0 || i == B_DO_EMPTY1 || i == B_DKDV_FULL;
+      const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DKDV_EMPTY)
+                               ? 256u : (i >= B_PX0 ? 64u : (both ? 2u : 1u));
       mbar_init(bar(i), cnt);
     }
     fence_barrier_init();
@@ -148,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
-    prefetch_tmap(&tmDQ);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
@@ -194,12 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = load_q(bh, block_at(first, 0, p));
         for (int ii = 0; ii < count && ok; ++ii) {
           const int blk = block_at(first, ii, p);
-          ok = mbar_wait(bar(B_DO_EMPTY), (dc & 1) ^ 1, abort_flag, p.err);
+          const uint32_t dst = dc & 1, duse = dc >> 1;
+          ok = mbar_wait(bar(B_DO_EMPTY0 + dst), (duse & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar(B_DO_FULL), C::kTileBytes);
+          mbar_arrive_expect_tx(bar(B_DO_FULL0 + dst), C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(base + C::kOffDO + c * C::kChunkBytes, &tmDO, bar(B_DO_FULL), 64 * c,
-                        blk * kBlk, bh);
+            tma_load_3d(base + C::kOffDO + dst * C::kTileBytes + c * C::kChunkBytes, &tmDO,
+                        bar(B_DO_FULL0 + dst), 64 * c, blk * kBlk, bh);
           ++dc;
           if (ii + 1 < count) ok = load_q(bh, block_at(first, ii + 1, p));
         }
@@ -208,117 +213,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it > 0) mbar_wait(bar(B_KV_FULL), (it - 1) & 1, abort_flag, p.err);
       for (uint32_t i = (qc > 2 ? qc - 2 : 0); i < qc; ++i)
         mbar_wait(bar(B_Q_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
-      if (dc > 0) mbar_wait(bar(B_DO_FULL), (dc - 1) & 1, abort_flag, p.err);
+      for (uint32_t i = (dc > 2 ? dc - 2 : 0); i < dc; ++i)
+        mbar_wait(bar(B_DO_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
+      const bool ia = warp == 1;  // A: dV, S^T   B: dK, dP^T
       constexpr uint32_t idSS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T, dP^T
       constexpr uint32_t idKM = idesc_bf16_f32(kBlk, D, true, false);      // dV, dK
-      constexpr uint32_t idMM = idesc_bf16_f32(kBlk, D, true, true);       // dQ
-      const uint32_t sK = base + C::kOffK, sV = base + C::kOffV, sDO = base + C::kOffDO;
-      const uint32_t sDS = base + C::kOffDS;
+      // stream A reads K and writes S^T; stream B reads V and writes dP^T
+      const uint32_t sKV = base + (ia ? C::kOffK : C::kOffV);
+      const uint32_t tScore = tbase + (ia ? C::kTmemS : C::kTmemDP);
+      const uint32_t tAcc = tbase + (ia ? C::kTmemDV : C::kTmemDK);
       uint32_t qc = 0;  // query blocks processed (global)
       int it = 0;
       bool ok = true, issued = false;
       auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
-      auto issue_s = [&](uint32_t c) -> bool {  // S^T_c = K Q_c^T
+      // the score tile of block c: A: S^T_c = K Q_c^T, B: dP^T_c = V dO_c^T
+      auto issue_score = [&](uint32_t c) -> bool {
         const uint32_t st = c & 1;
-        if (!w(bar(B_Q_FULL0 + st), (c >> 1) & 1)) return false;
+        if (!w(bar((ia ? B_Q_FULL0 : B_DO_FULL0) + st), (c >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t sQ = base + C::kOffQ + st * C::kTileBytes;
+        const uint32_t sB = base + (ia ? C::kOffQ : C::kOffDO) + st * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tbase + C::kTmemS, smem_desc_sw128(sK + off, 16, 1024),
-                 smem_desc_sw128(sQ + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
+          mma_ss(tScore, smem_desc_sw128(sKV + off, 16, 1024), smem_desc_sw128(sB + off, 16, 1024),
+                 idSS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(bar(B_S_FULL));
+        mma_commit(bar(ia ? B_S_FULL : B_DP_FULL));
         issued = true;
-        return true;
-      };
-      auto issue_dp = [&](uint32_t c) -> bool {  // dP^T_c = V dO_c^T (after dQ_{c-1} drained)
-        if (!w(bar(B_DO_FULL), c & 1)) return false;
-        if (c > 0 && !w(bar(B_DQ_EMPTY), (c - 1) & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tbase + C::kTmemDP, smem_desc_sw128(sV + off, 16, 1024),
-                 smem_desc_sw128(sDO + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(B_DP_FULL));
         return true;
       };
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, kb, first, count;
         bwd_item(idx, p, bh, kb, first, count);
-        ok = w(bar(B_KV_FULL), it & 1) && issue_s(qc) && issue_dp(qc);
+        ok = w(bar(B_KV_FULL), it & 1) && issue_score(qc);
         for (int ii = 0; ii < count && ok; ++ii, ++qc) {
           const uint32_t st = qc & 1;
-          const uint32_t sQ = base + C::kOffQ + st * C::kTileBytes;
-          // dV += P^T dO
-          if (!(ok = w(bar(B_P_FULL), qc & 1))) break;
+          // A: dV += P^T dO (P^T at [0,32) + [64,96));  B: dK += dS^T Q (dS^T at
+          // [128,160) + [192,224)); the B operand is the tile the other stream scored
+          if (!(ok = w(bar(ia ? B_P_FULL : B_DS_FULL), qc & 1))) break;
+          if (!(ok = w(bar((ia ? B_DO_FULL0 : B_Q_FULL0) + st), (qc >> 1) & 1))) break;
           if (ii == 0 && !(ok = w(bar(B_DKDV_EMPTY), (it & 1) ^ 1))) break;
           tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks)  // P^T halves at columns [0,32), [64,96)
-            mma_ts(tbase + C::kTmemDV, tbase + C::kTmemS + (ks < 4 ? 8 * ks : 32 + 8 * ks),
-                   smem_desc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idKM,
-                   (ii > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(B_DO_EMPTY));
-          if (ii + 1 < count && !(ok = issue_s(qc + 1))) break;
-          // dQ = dS K, then dK += dS^T Q
-          if (!(ok = w(bar(B_DS_FULL), qc & 1))) break;
-          tc_fence_after();
+          const uint32_t sB = base + (ia ? C::kOffDO : C::kOffQ) + st * C::kTileBytes;
 #pragma unroll
           for (int ks = 0; ks < kBlk / 16; ++ks)
-            mma_ss(tbase + C::kTmemDP, smem_desc_sw128(sDS + ks * 2048, C::kChunkBytes, 1024),
-                   smem_desc_sw128(sK + ks * 2048, C::kChunkBytes, 1024), idMM,
-                   ks > 0 ? 1u : 0u);
-          mma_commit(bar(B_DQ_FULL));
-#pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-            mma_ss(tbase + C::kTmemDK, smem_desc_sw128(sDS + off, 16, 1024),
-                   smem_desc_sw128(sQ + ks * 2048, C::kChunkBytes, 1024), idKM,
+            mma_ts(tAcc, tScore + (ks < 4 ? 8 * ks : 32 + 8 * ks),
+                   smem_desc_sw128(sB + ks * 2048, C::kChunkBytes, 1024), idKM,
                    (ii > 0 || ks > 0) ? 1u : 0u);
-          }
+          // Q_c is read by S^T_c (A) and dK_c (B); dO_c by dP^T_c (B) and dV_c (A): this
+          // stream's last read of either tile of block c is now issued
           mma_commit(bar(B_Q_EMPTY0 + st));
-          mma_commit(bar(B_DS_EMPTY));
-          if (ii + 1 < count && !(ok = issue_dp(qc + 1))) break;
+          mma_commit(bar(B_DO_EMPTY0 + st));
+          if (ii + 1 < count && !(ok = issue_score(qc + 1))) break;
         }
         if (!ok) break;
         mma_commit(bar(B_KV_EMPTY));
         mma_commit(bar(B_DKDV_FULL));
       }
       if (issued) {
-        mma_commit(bar(B_DRAIN));
-        mbar_wait(bar(B_DRAIN), 0, abort_flag, p.err);
+        const uint32_t dr = bar(ia ? B_DRAIN : B_DRAIN_B);
+        mma_commit(dr);
+        mbar_wait(dr, 0, abort_flag, p.err);
       }
     }
   } else {
     // ------------------------------------------------------------ compute warpgroups
-    // Two warpgroups, h = 0 (warps 2-5) and h = 1 (warps 6-9); each thread owns one key
+    // Two warpgroups, h = 0 (warps 3-6) and h = 1 (warps 7-10); each thread owns one key
     // row (TMEM lane) and query columns [64h, 64h + 64) of every block:
     //   P phase   P^T = exp2(S^T qk_scale - lse) -> bf16 into TMEM columns [64h, 64h+32)
-    //   dS phase  dS^T = P^T o (dP^T - Delta) -> bf16 into chunk h of the dS^T smem tile
-    //   drain     dQ_b columns [hD/2, (h+1)D/2) (one thread per query row) -> TMA
-    //             reduce-add through a 64-byte-swizzled 2 KB staging box per warp
+    //   dS phase  dS^T = P^T o (dP^T - Delta) -> bf16 into TMEM columns [128+64h, +32)
     //   epilogue  h = 0 stores dV, h = 1 stores dK (x sm_scale) for the item's key rows.
-    const int h = (warp - 2) >> 2;
+    const int h = (warp - 3) >> 2;
     const int quarter = warp & 3;
-    const int r = 32 * quarter + lane;               // key row (and query row in the drain)
+    const int r = 32 * quarter + lane;               // key row (TMEM lane)
     const uint32_t lrow = (32u * quarter) << 16;
     const float qk = p.a.qk_scale;
     auto wwait = [&](uint32_t b_, uint32_t par) {
       const bool okw = mbar_wait(b_, par, abort_flag, p.err);
       return __all_sync(0xffffffffu, okw) != 0;
     };
-    const uint32_t dsrow = base + C::kOffDS + h * C::kChunkBytes + r * 128;
-    const uint32_t sw = static_cast<uint32_t>(r & 7);
-    const uint32_t stage = base + C::kOffStage + (warp - 2) * 2048;
-    constexpr int kDrainCols = D / 2;
     uint32_t Pp[32];                                  // P^T of the current block, bf16 pairs
     // P phase of block `blk` (global index c): P^T -> TMEM for the dV MMA
     auto p_phase = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
@@ -337,15 +314,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 64; i += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float pv[4];
+          const float2 x0 = fma_rn_f32x2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])),
+                                         make_float2(qk, qk), make_float2(-l4.x, -l4.y));
+          const float2 x1 = fma_rn_f32x2(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])),
+                                         make_float2(qk, qk), make_float2(-l4.z, -l4.w));
+          Pp[i / 2] = pack_bf16x2(ex2f(x0.x), ex2f(x0.y));
+          Pp[i / 2 + 1] = pack_bf16x2(ex2f(x1.x), ex2f(x1.y));
+        }
+        // keys past Nkv (whole rows) and queries before the key on the causal diagonal
+        // get P = 0; a separate pass, taken only by the few rows and blocks that need it
+        if (__any_sync(0xffffffffu, !key_ok) || diag) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pv[e] = ex2f(fmaf(__uint_as_float(sr[i + e]), qk, -lv[e]));
-            if (!key_ok || (diag && qh + i + e < key)) pv[e] = 0.f;
+          for (int i = 0; i < 32; ++i) {
+            const bool m0 = !key_ok || (diag && qh + 2 * i < key);
+            const bool m1 = !key_ok || (diag && qh + 2 * i + 1 < key);
+            Pp[i] &= (m0 ? 0xffff0000u : 0xffffffffu) & (m1 ? 0x0000ffffu : 0xffffffffu);
           }
-          Pp[i / 2] = pack_bf16x2(pv[0], pv[1]);
-          Pp[i / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
         }
       }
       tmem_st16(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<const uint32_t(*)[16]>(&Pp[0]));
@@ -378,16 +362,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 64; i += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float pv = ex2f(fmaf(__uint_as_float(pf[i + e]), qk, -lv[e]));
-          if (!key_ok || (diag && qh + i + e < key)) pv = 0.f;
-          pf[i + e] = __float_as_uint(pv);
-        }
-        Pp[i / 2] = pack_bf16x2(__uint_as_float(pf[i]), __uint_as_float(pf[i + 1]));
-        Pp[i / 2 + 1] = pack_bf16x2(__uint_as_float(pf[i + 2]), __uint_as_float(pf[i + 3]));
+        const float2 x0 = fma_rn_f32x2(make_float2(__uint_as_float(pf[i]), __uint_as_float(pf[i + 1])),
+                                       make_float2(qk, qk), make_float2(-l4.x, -l4.y));
+        const float2 x1 = fma_rn_f32x2(make_float2(__uint_as_float(pf[i + 2]), __uint_as_float(pf[i + 3])),
+                                       make_float2(qk, qk), make_float2(-l4.z, -l4.w));
+        pf[i] = __float_as_uint(ex2f(x0.x));
+        pf[i + 1] = __float_as_uint(ex2f(x0.y));
+        pf[i + 2] = __float_as_uint(ex2f(x1.x));
+        pf[i + 3] = __float_as_uint(ex2f(x1.y));
       }
+      if (__any_sync(0xffffffffu, !key_ok) || diag) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (!key_ok || (diag && qh + i < key)) pf[i] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 64; i += 2)
+        Pp[i / 2] = pack_bf16x2(__uint_as_float(pf[i]), __uint_as_float(pf[i + 1]));
       // column maxima over this warp's 32 keys (non-negative floats order as their bits)
       uint32_t mine0 = 0u, mine1 = 0u;
 #pragma unroll
@@ -405,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float a0 = fmaxf(__uint_as_float(mine0), slot[(wip ^ 1) * 64 + lane]);
       const float a1 = fmaxf(__uint_as_float(mine1), slot[(wip ^ 1) * 64 + 32 + lane]);
       const TileScale t0 = tile_scale(a0), t1 = tile_scale(a1);
-      float* ws = psc + (warp - 2) * 128;              // inv [0,64), scale [64,128)
+      float* ws = psc + (warp - 3) * 128;              // inv [0,64), scale [64,128)
       ws[lane] = t0.inv;
       ws[32 + lane] = t1.inv;
       ws[64 + lane] = t0.scale;
@@ -429,13 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(B_P_FULL));
       return true;
     };
-    // dS phase of block c: dS^T = P^T o (dP^T - Delta) -> bf16 into the dS^T smem tile
+    // dS phase of block c: dS^T = P^T o (dP^T - Delta) -> bf16 over this group's dP^T
+    // columns (each 32-column load is consumed before the 16 packed columns it becomes
+    // are written; dP^T_{c+1} overwrites them only after dK_c has read them)
     auto ds_phase = [&](uint32_t c) -> bool {
       const float* sd =
           reinterpret_cast<const float*>(gbase + C::kOffDelta + (c & 1) * 512) + 64 * h;
-      bool okd = wwait(bar(B_DP_FULL), c & 1);
-      if (okd && c > 0) okd = wwait(bar(B_DS_EMPTY), (c - 1) & 1);
-      if (!okd) return false;
+      if (!wwait(bar(B_DP_FULL), c & 1)) return false;
       tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -456,61 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i / 2] = pack_bf16x2(ds[0], ds[1]);
           pk[i / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        // queries [32cc, 32cc + 32) of chunk h are 16-byte units 4cc .. 4cc + 3 of this
-        // row, each at its 128-byte-swizzled position (unit ^ row % 8)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t unit = static_cast<uint32_t>(4 * cc + u) ^ sw;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dsrow + unit * 16),
-                       "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
-                       : "memory");
-        }
+        tmem_st16(tbase + lrow + C::kTmemDP + 64 * h + 16 * cc, pk);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_DS_FULL));
-      return true;
-    };
-    // drain of block c: this group's dQ columns out of TMEM (TMEM freed at once), then
-    // TMA reduce-add into the fp32 accumulator, 16 rows x 32 columns per box
-    auto drain = [&](uint32_t c, int blk, int bh) -> bool {
-      if (!wwait(bar(B_DQ_FULL), c & 1)) return false;
-      tc_fence_after();
-      uint32_t o[kDrainCols];
-#pragma unroll
-      for (int cc = 0; cc < kDrainCols / 32; ++cc)
-        tmem_ld32(tbase + lrow + C::kTmemDP + kDrainCols * h + 32 * cc,
-                  *reinterpret_cast<uint32_t(*)[32]>(&o[32 * cc]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(B_DQ_EMPTY));
-      const int qrow0 = blk * kBlk + 32 * quarter;     // first query row of this warp
-      // boxes of 16 rows x 32 columns (128-byte rows, 128-byte swizzle): the TMA cost
-      // grows with the number of row segments, so wide rows halve it against 64 bytes
-#pragma unroll
-      for (int cc = 0; cc < kDrainCols / 32; ++cc) {
-#pragma unroll
-        for (int rh = 0; rh < 2; ++rh) {
-          if (lane == 0) bulk_wait_read_all();         // previous box has left the staging
-          __syncwarp();
-          if ((lane >> 4) == rh) {                     // the 16 lanes that own these rows
-            const uint32_t row = stage + (lane & 15) * 128;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                           ::"r"(row + ((u ^ (lane & 7)) * 16)),
-                           "r"(o[32 * cc + 4 * u]), "r"(o[32 * cc + 4 * u + 1]),
-                           "r"(o[32 * cc + 4 * u + 2]), "r"(o[32 * cc + 4 * u + 3])
-                           : "memory");
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-          if (lane == 0 && qrow0 + 16 * rh < p.a.Nq) {  // boxes past Nq hold no rows
-            tma_reduce_add_3d(&tmDQ, stage, kDrainCols * h + 32 * cc, qrow0 + 16 * rh, bh);
-            bulk_commit_group();
-          }
-        }
-      }
       return true;
     };
     uint32_t qc = 0;
@@ -521,18 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bwd_item(idx, p, bh, kb, first, count);
       const int key = kb * kBlk + r;
       const bool key_ok = key < p.a.Nkv;
-      // order per block b: dS_b, P_{b+1}, drain_b -- the next block's P is ready for its
-      // dV MMA before dQ_b has finished, and the reduce-add leaves the critical path
+      // order per block b: dS_b, then P_{b+1}, which is ready before dV_{b+1} is issued
       auto pp = [&](uint32_t c_, int blk_) {
         return p.a.page_bwd ? p_phase_page(c_, blk_, kb, key_ok, key)
                             : p_phase(c_, blk_, kb, key_ok, key);
       };
       ok = pp(qc, block_at(first, 0, p));
       for (int ii = 0; ii < count && ok; ++ii, ++qc) {
-        const int blk = block_at(first, ii, p);
         ok = ds_phase(qc);
         if (ok && ii + 1 < count) ok = pp(qc + 1, block_at(first, ii + 1, p));
-        if (ok) ok = drain(qc, blk, bh);
       }
       if (!ok) break;
       // ---- epilogue: h = 0 stores dV, h = 1 stores dK for this item's key rows
@@ -563,8 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(B_DKDV_EMPTY));
     }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -574,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ small kernels
 
-// One warp per padded query row: Delta, lse copy (+inf in padding), dQ accumulator = 0.
+// One warp per padded query row: Delta and the lse copy (+inf in padding rows).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
   constexpr int PER = D / 32;
@@ -606,14 +542,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
         acc = fmaf(of.x, df.x, acc);
         acc = fmaf(of.y, df.y, acc);
       }
-      *reinterpret_cast<float4*>(a.dq_acc + src) = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
       const uint32_t ov = *reinterpret_cast<const uint32_t*>(a.o_hp + src);
       const uint32_t dv = *reinterpret_cast<const uint32_t*>(a.dO + src);
       const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
       const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv));
       acc = fmaf(of.x, df.x, of.y * df.y);
-      *reinterpret_cast<float2*>(a.dq_acc + src) = make_float2(0.f, 0.f);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -621,21 +555,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
       a.delta[rw] = acc;
       a.lse_pad[rw] = a.lse[bh * a.Nq + q];
     }
-  }
-}
-
-// dQ = bf16(dQ_acc * sm_scale), 8 elements per thread-step.
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
-                                                         uint16_t* __restrict__ dq, float scale,
-                                                         long long n8) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += stride) {
-    const float4 x = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 y = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    reinterpret_cast<uint4*>(dq)[i] =
-        make_uint4(pack_bf16x2(x.x * scale, x.y * scale), pack_bf16x2(x.z * scale, x.w * scale),
-                   pack_bf16x2(y.x * scale, y.y * scale), pack_bf16x2(y.z * scale, y.w * scale));
   }
 }
 
@@ -658,24 +577,18 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  CUtensorMap mq, mk, mv, mdo;
   if (!make_bf16_map_3d(&mq, a.q, D, a.Nq, BH) || !make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) ||
-      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) || !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH) ||
-      !make_f32_map_3d(&mdq, a.dq_acc, D, a.Nq, BH))
+      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) || !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH))
     return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = p.items < num_sms ? p.items : num_sms;
-  attn_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, mdq, p);
+  attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-
-  const long long n8 = static_cast<long long>(BH) * a.Nq * D / 8;
-  long long cblocks = (n8 + 255) / 256;
-  if (cblocks > static_cast<long long>(num_sms) * 32) cblocks = static_cast<long long>(num_sms) * 32;
-  dq_convert_kernel<<<static_cast<unsigned>(cblocks), 256, 0, s>>>(a.dq_acc, a.dq, a.sm_scale, n8);
-  return cudaGetLastError();
+  return launch_bwd_dq(a, err, num_sms, s);
 }
 
 }  // namespace

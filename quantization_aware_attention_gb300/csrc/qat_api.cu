@@ -210,7 +210,7 @@ qat_status_t qat_attn_merge(float* o_q_acc, float* o_hp_acc, float* lse_acc,
 size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D) {
   bool empty = false;
   if (check_sizes(B, H, Nq, Nkv, D, 1.0f, 0, 0, &empty) != QAT_OK) return 0;
-  return qat::bwd_workspace_layout(B, H, Nq, D).total;
+  return qat::bwd_workspace_layout(B, H, Nq).total;
 }
 
 qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const void* o_hp,
@@ -239,7 +239,7 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return QAT_ERR_INVALID_ARG;
 
   qat::BwdArgs a;
-  const qat::BwdWorkspace wl = qat::bwd_workspace_layout(B, H, Nq, D);
+  const qat::BwdWorkspace wl = qat::bwd_workspace_layout(B, H, Nq);
   char* ws = static_cast<char*>(workspace);
   a.q = static_cast<const uint16_t*>(q);
   a.k = static_cast<const uint16_t*>(k);
@@ -252,7 +252,6 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.dv = static_cast<uint16_t*>(dv);
   a.lse_pad = reinterpret_cast<float*>(ws + wl.off_lse);
   a.delta = reinterpret_cast<float*>(ws + wl.off_delta);
-  a.dq_acc = reinterpret_cast<float*>(ws + wl.off_dq);
   a.B = B; a.H = H; a.Nq = Nq; a.Nkv = Nkv; a.D = D;
   a.sm_scale = sm_scale;
   a.qk_scale = sm_scale * kLog2e;

@@ -8,21 +8,20 @@
 
 namespace qat {
 
-// Backward workspace: [lse_pad | delta | dq_acc], each piece 256-byte aligned; query rows
-// are padded per head to a multiple of 128 for lse_pad and delta.
+// Backward workspace: [lse_pad | delta], each piece 256-byte aligned; query rows are
+// padded per head to a multiple of 128.
 struct BwdWorkspace {
-  size_t nq_pad, off_lse, off_delta, off_dq, total;
+  size_t nq_pad, off_lse, off_delta, total;
 };
 
-inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int D) {
+inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   BwdWorkspace w;
   w.nq_pad = (static_cast<size_t>(Nq) + 127) / 128 * 128;
   const size_t rows_pad = static_cast<size_t>(B) * H * w.nq_pad;
   w.off_lse = 0;
   w.off_delta = up(rows_pad * sizeof(float));
-  w.off_dq = w.off_delta + up(rows_pad * sizeof(float));
-  w.total = w.off_dq + up(static_cast<size_t>(B) * H * Nq * D * sizeof(float));
+  w.total = w.off_delta + up(rows_pad * sizeof(float));
   if (w.total == 0) w.total = 256;
   return w;
 }
@@ -31,8 +30,6 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int D) {
 // 128-byte swizzle, zero fill out of bounds.
 bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH,
                       int head_rows = -1);
-// [BH, N, D] fp32 as a 3-D TMA tensor with 32 x 16 x 1 boxes (128-byte rows, swizzled).
-bool make_f32_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH);
 
 // Arguments of one forward launch (device pointers, validated by the ABI layer).
 struct FwdArgs {
@@ -65,7 +62,6 @@ struct BwdArgs {
   uint16_t* dv;
   float* delta;     // fp32 [B, H, Nq_pad] in the workspace (0 in padding rows)
   float* lse_pad;   // fp32 [B, H, Nq_pad] copy of lse (+inf in padding rows)
-  float* dq_acc;    // fp32 [B, H, Nq, D] dQ accumulator in the workspace
   int B, H, Nq, Nkv, D;
   float sm_scale;
   float qk_scale;
@@ -75,7 +71,9 @@ struct BwdArgs {
 
 // Kernel launchers (return cudaGetLastError() after the launches).
 cudaError_t launch_fwd_tc(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
+// prep + dK/dV + dQ kernels
 cudaError_t launch_bwd_tc(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
 cudaError_t launch_channel_mean(const uint16_t* x, float* mean, long long rows, int D,
                                 int num_sms, cudaStream_t s);
 cudaError_t launch_fake_quant_tokens(const uint16_t* x, const float* mean, uint16_t* out,
