@@ -11,23 +11,22 @@
 // passes the gradient of O_q through the quantizer as the identity.
 //
 // CTA layout (352 threads, one CTA per SM, persistent over (head, 128-row query block)):
-//   warp 0      TMA producer: K_j (3-stage ring) and V_j (3-stage ring), 128 keys x D.
-//   warps 1, 2  MMA issuers (lane 0 of each), all MMAs with A in TMEM:
-//                 warp 1:  S  = Q K_j^T   (A = Q bf16 in TMEM, B = K_j K-major)  -> TMEM S
-//                 warp 2:  dQ += dS K_j   (A = dS bf16 in TMEM, B = K_j MN-major), then
-//                          dP = dO V_{j+1}^T (A = dO bf16 in TMEM, B = V K-major) -> dP
-//               One thread issues at most one MMA per ~93 cycles on this GPU, well under
-//               the tensor core's rate for M = 128, N = 128; two issuing warps keep it
-//               busy.  Each stream is ordered on its own; dP_{j+1} overwrites the dS_j
-//               that dQ_j reads, so both sit in warp 2's stream.  Warp 1 also owns TMEM.
-//   warps 3-10  two compute warpgroups; group h owns keys [64h, 64h + 64) of every
-//               block, each thread one query row (TMEM lane).  Per item they copy the
-//               Q rows (h = 0) or dO rows (h = 1) into TMEM, and at the end store their
-//               half of dQ's columns.  dS is written over the group's own dP columns.
-// Only the MMAs read shared memory (the B operands), which keeps the shared-memory
-// traffic per block at a fraction of an all-SS design.
-// TMEM (512 columns): S [0,128), dP / dS [128,256), dQ [256,256+D), Q [256+D, 256+3D/2),
-// dO [256+3D/2, 256+2D).
+//   warp 0      TMA producer: the item's dO tile, then K_j and V_j (3-stage rings each),
+//               128 rows x D in 128-byte-swizzled boxes.
+//   warp 1      TMEM owner; lane 0 issues, in this order, S_{j+1} then dQ_j:
+//                 S  = Q K^T      TS  (A = Q bf16 in TMEM, B = K_j K-major)   -> TMEM S
+//                 dQ += dS K      TS  (A = dS bf16 in TMEM, B = K_j MN-major) -> TMEM dQ
+//   warp 2      lane 0 issues dP = dO V^T (SS, A = dO K-major, B = V_j K-major) -> TMEM dP
+//               as soon as the compute warps have read the previous dP.
+//               One thread issues at most one MMA per ~93 cycles on this GPU, so the
+//               products come from two issuers.  S, dP and dS each have their own TMEM
+//               columns, so no product waits for another block's dQ.
+//   warps 3-10  two compute warpgroups; group h owns keys [64h, 64h + 64) of every block,
+//               each thread one query row (TMEM lane): P from S, dS from P and dP into
+//               the dS columns, and at the end half of dQ's columns to global memory.
+//               Per item they also copy their half of each Q row into TMEM.
+// TMEM (512 columns for D = 128): S [0,128), dP [128,256), dQ [256,256+D),
+// Q [256+D, 256+3D/2), dS [256+3D/2, 256+3D/2+64).
 #include "qat_internal.h"
 #include "qat_quant.cuh"
 #include "sm100.cuh"
@@ -51,7 +50,8 @@ struct BwdDq {
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t kChunkBytes = kBlk * 128;      // 16 KB box: 128 rows x 128 B
   static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
-  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffDO = 0;
+  static constexpr uint32_t kOffK = kOffDO + kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr uint32_t kOffMisc = kOffBar + 256;
@@ -59,14 +59,18 @@ struct BwdDq {
   // at least 116 KB so that no two CTAs share an SM (each holds all 512 TMEM columns)
   static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
-  static constexpr uint32_t kTmemQ = 256 + D, kTmemDO = 256 + D + D / 2;
+  static constexpr uint32_t kTmemQ = 256 + D, kTmemDS = 256 + D + D / 2;
 };
+static_assert(BwdDq<128>::kSmemBytes <= 232448u, "shared memory budget");
+static_assert(BwdDq<128>::kTmemDS + 64 <= 512u, "TMEM budget");
 
 enum : uint32_t {
   Q_K_FULL = 0, Q_K_EMPTY = Q_K_FULL + kKStages, Q_V_FULL = Q_K_EMPTY + kKStages,
-  Q_V_EMPTY = Q_V_FULL + kVStages, Q_S_FULL = Q_V_EMPTY + kVStages, Q_S_EMPTY, Q_DP_FULL,
-  Q_DS_FULL, Q_QD_FULL, Q_QD_EMPTY, Q_DQ_FULL, Q_DQ_EMPTY, Q_DRAIN_A, Q_DRAIN_B, Q_COUNT
+  Q_V_EMPTY = Q_V_FULL + kVStages, Q_DO_FULL = Q_V_EMPTY + kVStages, Q_DO_EMPTY, Q_S_FULL,
+  Q_S_EMPTY, Q_DP_FULL, Q_DP_EMPTY, Q_DS_FULL, Q_DS_FREE, Q_QR_FULL, Q_QR_EMPTY, Q_DQ_FULL,
+  Q_DQ_EMPTY, Q_DRAIN_A, Q_DRAIN_B, Q_COUNT
 };
+static_assert(Q_COUNT <= 32, "barrier block");
 
 struct DqParams {
   BwdArgs a;
@@ -104,7 +108,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const DqParams p) {
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmDO, const DqParams p) {
   using C = BwdDq<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -119,14 +124,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     *abort_flag = 0;
     for (uint32_t i = 0; i < Q_COUNT; ++i) {
-      const bool wg = i == Q_S_EMPTY || i == Q_DS_FULL || i == Q_QD_FULL || i == Q_DQ_EMPTY;
-      // K tiles and the item's Q / dO rows are read by both issuers: one commit from each
-      const bool both = (i >= Q_K_EMPTY && i < Q_K_EMPTY + kKStages) || i == Q_QD_EMPTY;
-      mbar_init(bar(i), wg ? 256u : (both ? 2u : 1u));
+      const bool wg = i == Q_S_EMPTY || i == Q_DP_EMPTY || i == Q_DS_FULL || i == Q_QR_FULL ||
+                      i == Q_DQ_EMPTY;
+      mbar_init(bar(i), wg ? 256u : 1u);
     }
     fence_barrier_init();
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
@@ -141,10 +146,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t kc = 0, vc = 0;
+      int it = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x) {
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, mt, J;
         dq_item(idx, p, bh, mt, J);
+        ok = mbar_wait(bar(Q_DO_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(Q_DO_FULL), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(base + C::kOffDO + c * C::kChunkBytes, &tmDO, bar(Q_DO_FULL), 64 * c,
+                      mt * kBlk, bh);
         for (int j = 0; j < J && ok; ++j) {
           {
             const uint32_t st = kc % kKStages, use = kc / kKStages;
@@ -169,40 +181,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // drain: every issued load lands before the CTA exits
+      if (it > 0) mbar_wait(bar(Q_DO_FULL), (it - 1) & 1, abort_flag, p.err);
       for (uint32_t i = (kc > kKStages ? kc - kKStages : 0); i < kc; ++i)
         mbar_wait(bar(Q_K_FULL + i % kKStages), (i / kKStages) & 1, abort_flag, p.err);
       for (uint32_t i = (vc > kVStages ? vc - kVStages : 0); i < vc; ++i)
         mbar_wait(bar(Q_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.err);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer A: S
+    // ------------------------------------------------------------ MMA issuer A: S, dQ
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(kBlk, kBlk, false);
+      constexpr uint32_t idS = idesc_bf16_f32(kBlk, kBlk, false);  // S (B = K K-major)
+      constexpr uint32_t idQ = idesc_bf16_f32(kBlk, D, true);      // dQ (B = K MN-major)
       uint32_t kc = 0, bc = 0;  // K tiles, blocks (global counts)
       int it = 0;
       bool ok = true, issued = false;
       auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
+      // S of block c (K tile k): after the compute warps have read S of block c - 1
+      auto issue_s = [&](uint32_t k, uint32_t c, bool last) -> bool {
+        if (c > 0 && !w(bar(Q_S_EMPTY), (c - 1) & 1)) return false;
+        const uint32_t st = k % kKStages;
+        if (!w(bar(Q_K_FULL + st), (k / kKStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          mma_ts(tbase + C::kTmemS, tbase + C::kTmemQ + 8 * ks,
+                 smem_desc_sw128(sk + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+        }
+        issued = true;
+        mma_commit(bar(Q_S_FULL));
+        if (last) mma_commit(bar(Q_QR_EMPTY));  // the item's last read of its Q rows
+        return true;
+      };
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, mt, J;
         dq_item(idx, p, bh, mt, J);
-        ok = w(bar(Q_QD_FULL), it & 1);  // this item's Q and dO rows are in TMEM
+        ok = w(bar(Q_QR_FULL), it & 1) && issue_s(kc, bc, J == 1);
         for (int j = 0; j < J && ok; ++j, ++kc, ++bc) {
-          // S_j overwrites S_{j-1}: wait until the compute warps have read it
-          if (bc > 0 && !(ok = w(bar(Q_S_EMPTY), (bc - 1) & 1))) break;
-          const uint32_t st = kc % kKStages;
-          if (!(ok = w(bar(Q_K_FULL + st), (kc / kKStages) & 1))) break;
+          if (j + 1 < J && !(ok = issue_s(kc + 1, bc + 1, j + 2 == J))) break;
+          // dQ += dS_j K_j, once the compute warps have written dS_j
+          if (!(ok = w(bar(Q_DS_FULL), bc & 1))) break;
+          if (j == 0 && it > 0 && !(ok = w(bar(Q_DQ_EMPTY), (it - 1) & 1))) break;
           tc_fence_after();
+          const uint32_t st = kc % kKStages;
           const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-            mma_ts(tbase + C::kTmemS, tbase + C::kTmemQ + 8 * ks,
-                   smem_desc_sw128(sk + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
-          }
-          issued = true;
-          mma_commit(bar(Q_S_FULL));
-          mma_commit(bar(Q_K_EMPTY + st));
-          if (j + 1 == J) mma_commit(bar(Q_QD_EMPTY));  // the item's last read of Q
+          for (int ks = 0; ks < kBlk / 16; ++ks)
+            mma_ts(tbase + C::kTmemDQ, tbase + C::kTmemDS + 8 * ks,
+                   smem_desc_sw128(sk + ks * 2048, C::kChunkBytes, 1024), idQ,
+                   (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(Q_K_EMPTY + st));  // K_j: read by S_j and dQ_j, both issued here
+          mma_commit(bar(Q_DS_FREE));
+          if (j + 1 == J) mma_commit(bar(Q_DQ_FULL));
         }
       }
       if (issued) {
@@ -211,57 +242,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ MMA issuer B: dQ, dP
+    // ------------------------------------------------------------ MMA issuer B: dP
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(kBlk, kBlk, false);  // dP
-      constexpr uint32_t idQ = idesc_bf16_f32(kBlk, D, true);      // dQ (B = K MN-major)
-      uint32_t kc = 0, vc = 0, bc = 0;  // K tiles, V tiles, blocks (global counts)
+      constexpr uint32_t idS = idesc_bf16_f32(kBlk, kBlk, false);
+      uint32_t vc = 0, bc = 0;
       int it = 0;
       bool ok = true, issued = false;
       auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
-      // dP = dO V^T into TMEM dP (after the previous dQ in this stream, which read dS there)
-      auto issue_dp = [&](uint32_t v, bool last) -> bool {
-        const uint32_t st = v % kVStages;
-        if (!w(bar(Q_V_FULL + st), (v / kVStages) & 1)) return false;
-        tc_fence_after();
-        const uint32_t sv = base + C::kOffV + st * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          mma_ts(tbase + C::kTmemDP, tbase + C::kTmemDO + 8 * ks,
-                 smem_desc_sw128(sv + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
-        }
-        issued = true;
-        mma_commit(bar(Q_V_EMPTY + st));
-        mma_commit(bar(Q_DP_FULL));
-        if (last) mma_commit(bar(Q_QD_EMPTY));  // the item's last read of dO
-        return true;
-      };
+      const uint32_t sdo = base + C::kOffDO;
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, mt, J;
         dq_item(idx, p, bh, mt, J);
-        ok = w(bar(Q_QD_FULL), it & 1) && issue_dp(vc, J == 1);
-        for (int j = 0; j < J && ok; ++j) {
-          // dQ += dS_j K_j: dS_j (keys [64g, 64g + 64) in group g's dP columns)
-          if (!(ok = w(bar(Q_DS_FULL), bc & 1))) break;
-          if (j == 0 && it > 0 && !(ok = w(bar(Q_DQ_EMPTY), (it - 1) & 1))) break;
+        ok = w(bar(Q_DO_FULL), it & 1);
+        for (int j = 0; j < J && ok; ++j, ++vc, ++bc) {
+          // dP overwrites dP of block bc - 1: wait until the compute warps have read it
+          if (bc > 0 && !(ok = w(bar(Q_DP_EMPTY), (bc - 1) & 1))) break;
+          const uint32_t st = vc % kVStages;
+          if (!(ok = w(bar(Q_V_FULL + st), (vc / kVStages) & 1))) break;
           tc_fence_after();
-          const uint32_t st = kc % kKStages;
-          const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
+          const uint32_t sv = base + C::kOffV + st * C::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks)
-            mma_ts(tbase + C::kTmemDQ, tbase + C::kTmemDP + (ks < 4 ? 8 * ks : 32 + 8 * ks),
-                   smem_desc_sw128(sk + ks * 2048, C::kChunkBytes, 1024), idQ,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(Q_K_EMPTY + st));
-          ++kc;
-          ++bc;
-          ++vc;
-          if (j + 1 < J) {
-            if (!(ok = issue_dp(vc, j + 2 == J))) break;
-          } else {
-            mma_commit(bar(Q_DQ_FULL));
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+            mma_ss(tbase + C::kTmemDP, smem_desc_sw128(sdo + off, 16, 1024),
+                   smem_desc_sw128(sv + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
           }
+          issued = true;
+          mma_commit(bar(Q_V_EMPTY + st));
+          mma_commit(bar(Q_DP_FULL));
+          if (j + 1 == J) mma_commit(bar(Q_DO_EMPTY));
         }
       }
       if (issued) {
@@ -280,29 +289,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool okw = mbar_wait(b_, par, abort_flag, p.err);
       return __all_sync(0xffffffffu, okw) != 0;
     };
-    // Q (h = 0) or dO (h = 1) row of this thread into TMEM as bf16 pairs; rows past Nq
+    // half h of this thread's Q row into TMEM as bf16 pairs (D / 4 columns); rows past Nq
     // are zero (their lse is +inf, so P = 0 there)
-    auto load_rows = [&](int bh, int mt) {
+    auto load_q = [&](int bh, int mt) {
+      constexpr int kCols = D / 4;
       const int row = mt * kBlk + r;
-      const uint16_t* src = (h ? p.a.dO : p.a.q) + (static_cast<size_t>(bh) * p.a.Nq + row) * D;
-      const uint32_t dst = tbase + lrow + (h ? C::kTmemDO : C::kTmemQ);
+      const uint16_t* src = p.a.q + (static_cast<size_t>(bh) * p.a.Nq + row) * D + (D / 2) * h;
+      uint32_t v[kCols];
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint4 x = make_uint4(0u, 0u, 0u, 0u);
-          if (row < p.a.Nq) x = *reinterpret_cast<const uint4*>(src + 64 * c + 8 * u);
-          v[4 * u] = x.x;
-          v[4 * u + 1] = x.y;
-          v[4 * u + 2] = x.z;
-          v[4 * u + 3] = x.w;
-        }
-        tmem_st32(dst + 32 * c, v);
+      for (int u = 0; u < kCols / 4; ++u) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (row < p.a.Nq) x = *reinterpret_cast<const uint4*>(src + 8 * u);
+        v[4 * u] = x.x;
+        v[4 * u + 1] = x.y;
+        v[4 * u + 2] = x.z;
+        v[4 * u + 3] = x.w;
       }
+      const uint32_t dst = tbase + lrow + C::kTmemQ + kCols * h;
+      if constexpr (kCols == 32)
+        tmem_st32(dst, v);
+      else
+        tmem_st16(dst, v);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(Q_QD_FULL));
+      mbar_arrive(bar(Q_QR_FULL));
     };
     uint32_t bc = 0;
     int it = 0;
@@ -310,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (static_cast<int>(blockIdx.x) < p.items) {
       int bh, mt, J;
       dq_item(blockIdx.x, p, bh, mt, J);
-      load_rows(bh, mt);
+      load_q(bh, mt);
     }
     for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
       int bh, mt, J;
@@ -347,36 +357,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = wwait(bar(Q_DP_FULL), bc & 1))) break;
         tc_fence_after();
+        uint32_t pk[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t dr[32];
           tmem_ld32(tbase + lrow + C::kTmemDP + 64 * h + 32 * cc, dr);
           tmem_wait_ld();
-          uint32_t pk[16];
+          if (cc == 1) {                               // every read of this dP is done
+            tc_fence_before();
+            mbar_arrive(bar(Q_DP_EMPTY));
+          }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float2 d = mul_rn_f32x2(
                 make_float2(__uint_as_float(pr[32 * cc + 2 * i]), __uint_as_float(pr[32 * cc + 2 * i + 1])),
                 add_rn_f32x2(make_float2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])),
                              make_float2(-delta_r, -delta_r)));
-            pk[i] = pack_bf16x2(d.x, d.y);
+            pk[16 * cc + i] = pack_bf16x2(d.x, d.y);
           }
-          // dS of keys [64h + 32cc, +32) over dP columns this thread has already read
-          tmem_st16(tbase + lrow + C::kTmemDP + 64 * h + 16 * cc, pk);
         }
+        // dS of keys [64h, 64h + 64) -> TMEM dS columns [32h, 32h + 32), once dQ of the
+        // previous block has read the buffer
+        if (bc > 0 && !(ok = wwait(bar(Q_DS_FREE), (bc - 1) & 1))) break;
+        tc_fence_after();
+        tmem_st32(tbase + lrow + C::kTmemDS + 32 * h, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(Q_DS_FULL));
       }
       if (!ok) break;
-      // the next item's Q / dO rows go in while this item's last dQ MMA runs
+      // the next item's Q rows go in once this item's last S has read the current ones
       const int nidx = idx + static_cast<int>(gridDim.x);
       if (nidx < p.items) {
-        if (!(ok = wwait(bar(Q_QD_EMPTY), it & 1))) break;
+        if (!(ok = wwait(bar(Q_QR_EMPTY), it & 1))) break;
         tc_fence_after();
         int nbh, nmt, nJ;
         dq_item(nidx, p, nbh, nmt, nJ);
-        load_rows(nbh, nmt);
+        load_q(nbh, nmt);
       }
       // ---- epilogue: group h stores dQ columns [hD/2, (h+1)D/2) of its row
       if (!(ok = wwait(bar(Q_DQ_FULL), it & 1))) break;
@@ -420,15 +437,16 @@ cudaError_t launch_bwd_dq_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   p.ntiles = (a.Nkv + kBlk - 1) / kBlk;
   p.items = BH * p.mtiles;
   p.nq_pad = p.mtiles * kBlk;
-  CUtensorMap mk, mv;
-  if (!make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) || !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH))
+  CUtensorMap mk, mv, mdo;
+  if (!make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) || !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) ||
+      !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = p.items < num_sms ? p.items : num_sms;
-  attn_bwd_dq_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mk, mv, p);
+  attn_bwd_dq_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mk, mv, mdo, p);
   return cudaGetLastError();
 }
 

@@ -7,21 +7,23 @@
 //   amax = max p, Pq = quant(p) (qat_quant.cuh);  O_q = alpha O_q + Pq V_j;
 //   O_hp = alpha O_hp + P V_j;  epilogue O / l, lse = m + log2 l.
 //
-// CTA layout (320 threads, one CTA per SM, persistent over (head, 128-row q tile)):
+// CTA layout (352 threads, one CTA per SM, persistent over (head, 128-row q tile)):
 //   warp 0      TMA producer: Q tile once per work item, K tiles (3-stage ring) and
 //               V tiles (2-stage ring), 128 keys x D, 128-byte swizzled boxes.
-//   warp 1      TMEM allocator; lane 0 issues every tcgen05.mma:
+//   warp 1      TMEM allocator; lane 0 issues the score MMAs:
 //                 S_j = Q K_j^T            (SS, M=128, N=128 keys, K=D) -> TMEM S[j%2]
+//   warp 2      lane 0 issues the value MMAs:
 //                 O_q += Pq_j V_j          (TS: A = Pq in TMEM, B = V MN-major in smem)
 //                 O_hp += P_j V_j          (TS, same V descriptors: the two P tiles share V)
-//               issue order S_j, PV_{j-1}, S_{j+1}, ... so the tensor core computes the
-//               next scores while the softmax warps work on the current tile.
-//   warps 2-9   softmax + quantization in two warpgroups: warps 2-5 take keys 0-63 and
-//               warps 6-9 keys 64-127 of each S row (one 64-key quantization tile per
+//               One thread issues at most one MMA per ~93 cycles on this GPU; two issuers
+//               keep the tensor core busy.  S_{j+2} reuses the buffer that holds P_j, so
+//               warp 1 waits for warp 2's commit of PV_j before issuing it.
+//   warps 3-10  softmax + quantization in two warpgroups: warps 3-6 take keys 0-63 and
+//               warps 7-10 keys 64-127 of each S row (one 64-key quantization tile per
 //               thread), exchanging the row max through shared memory.  P is written
 //               back into the S buffer it came from as two bf16 tiles (Pq in columns
-//               0-63, P in 64-127), consumed by the TS MMAs.  Epilogue: warps 2-5 store
-//               O_q and lse, warps 6-9 O_hp.
+//               0-63, P in 64-127), consumed by the TS MMAs.  Epilogue: warps 3-6 store
+//               O_q and lse, warps 7-10 O_hp.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O_q [256,256+D), O_hp [256+D,256+2D).
 //
 // The running max is updated only when it grows by more than 8 (base-2 units), so P
@@ -47,7 +49,7 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 
 template <int D>
@@ -72,7 +74,7 @@ struct FwdTc {
 enum : uint32_t {
   BAR_Q_FULL = 0, BAR_Q_EMPTY = 1, BAR_K_FULL = 2, BAR_K_EMPTY = 5, BAR_V_FULL = 8,
   BAR_V_EMPTY = 10, BAR_S_FULL = 12, BAR_P_FULL = 14, BAR_O_DONE = 16, BAR_O_EMPTY = 17,
-  BAR_DRAIN = 18, BAR_X = 19, BAR_COUNT = 20
+  BAR_DRAIN = 18, BAR_X = 19, BAR_S_FREE = 20, BAR_DRAIN_B = 22, BAR_COUNT = 23
 };
 
 struct TcParams {
@@ -146,10 +148,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(BAR_S_FULL + b), 1);
       mbar_init(bar(BAR_P_FULL + b), 256);
+      mbar_init(bar(BAR_S_FREE + b), 1);
     }
     mbar_init(bar(BAR_O_DONE), 1);
     mbar_init(bar(BAR_O_EMPTY), 256);
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_DRAIN_B), 1);
     mbar_init(bar(BAR_X), 256);
     fence_barrier_init();
     prefetch_tmap(&tmQ);
@@ -213,50 +217,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(BAR_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.err);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score MMAs (S = Q K^T)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false);
-      constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, true);
-      uint32_t kc = 0, vc = 0, sc = 0, pc = 0;
+      uint32_t kc = 0, sc = 0;
       int it = 0;
       bool ok = true, issued = false;
-      auto issue_pv = [&](bool first) -> bool {
-        const uint32_t b = pc & 1;
-        if (!mbar_wait(bar(BAR_P_FULL + b), (pc >> 1) & 1, abort_flag, p.err)) return false;
-        if (first && !mbar_wait(bar(BAR_O_EMPTY), (it & 1) ^ 1, abort_flag, p.err)) return false;
-        const uint32_t st = vc % kVStages;
-        if (!mbar_wait(bar(BAR_V_FULL + st), (vc / kVStages) & 1, abort_flag, p.err))
-          return false;
-        tc_fence_after();
-        const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
-        const uint32_t sP = tbase + b * 128;
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t dv = smem_desc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
-          mma_ts(tbase + C::kTmemOq, sP + 8 * ks, dv, idPV, (!first || ks > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t dv = smem_desc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
-          mma_ts(tbase + C::kTmemOhp, sP + 64 + 8 * ks, dv, idPV, (!first || ks > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(BAR_V_EMPTY + st));
-        mma_commit(bar(BAR_O_DONE));
-        ++vc;
-        ++pc;
-        return true;
-      };
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, mt;
         item_coords(idx, p, bh, mt);
         const int J = kv_tiles(p, mt);
         ok = mbar_wait(bar(BAR_Q_FULL), it & 1, abort_flag, p.err);
-        for (int j = 0; j < J && ok; ++j) {
+        for (int j = 0; j < J && ok; ++j, ++kc, ++sc) {
           const uint32_t st = kc % kKStages;
+          const uint32_t b = sc & 1;
           ok = mbar_wait(bar(BAR_K_FULL + st), (kc / kKStages) & 1, abort_flag, p.err);
+          // buffer b holds P of tile sc - 2 until its value MMAs have completed
+          if (ok && sc >= 2)
+            ok = mbar_wait(bar(BAR_S_FREE + b), ((sc - 2) >> 1) & 1, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t b = sc & 1;
           const uint32_t qb = base + C::kOffQ;
           const uint32_t kb = base + C::kOffK + st * C::kTileBytes;
 #pragma unroll
@@ -269,22 +249,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bar(BAR_K_EMPTY + st));
           mma_commit(bar(BAR_S_FULL + b));
           if (j == J - 1) mma_commit(bar(BAR_Q_EMPTY));
-          ++kc;
-          ++sc;
-          if (j >= 1) ok = issue_pv(j == 1);
         }
-        if (ok) ok = issue_pv(J == 1);
       }
       if (issued) {  // drain: wait until every MMA this thread issued has completed
         mma_commit(bar(BAR_DRAIN));
         mbar_wait(bar(BAR_DRAIN), 0, abort_flag, p.err);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ value MMAs (P V)
+    if (lane == 0) {
+      constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, true);
+      uint32_t vc = 0, pc = 0;
+      int it = 0;
+      bool ok = true, issued = false;
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, mt;
+        item_coords(idx, p, bh, mt);
+        const int J = kv_tiles(p, mt);
+        for (int j = 0; j < J && ok; ++j, ++vc, ++pc) {
+          const uint32_t b = pc & 1;
+          ok = mbar_wait(bar(BAR_P_FULL + b), (pc >> 1) & 1, abort_flag, p.err);
+          if (ok && j == 0) ok = mbar_wait(bar(BAR_O_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
+          const uint32_t st = vc % kVStages;
+          if (ok) ok = mbar_wait(bar(BAR_V_FULL + st), (vc / kVStages) & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
+          const uint32_t sP = tbase + b * 128;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            const uint64_t dv = smem_desc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
+            mma_ts(tbase + C::kTmemOq, sP + 8 * ks, dv, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            const uint64_t dv = smem_desc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
+            mma_ts(tbase + C::kTmemOhp, sP + 64 + 8 * ks, dv, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(bar(BAR_V_EMPTY + st));
+          mma_commit(bar(BAR_O_DONE));
+          mma_commit(bar(BAR_S_FREE + b));
+        }
+      }
+      if (issued) {
+        mma_commit(bar(BAR_DRAIN_B));
+        mbar_wait(bar(BAR_DRAIN_B), 0, abort_flag, p.err);
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    // Two warpgroups: h = 0 (warps 2-5) owns keys 0-63 of every S row, h = 1 (warps
-    // 6-9) keys 64-127 -- each thread one row of one 64-key quantization tile.
-    const int h = (warp - 2) >> 2;
+    // Two warpgroups: h = 0 (warps 3-6) owns keys 0-63 of every S row, h = 1 (warps
+    // 7-10) keys 64-127 -- each thread one row of one 64-key quantization tile.
+    const int h = (warp - 3) >> 2;
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int r = 32 * quarter + lane;            // row of the 128-row tile
     const uint32_t lrow = (32u * quarter) << 16;  // TMEM lane offset
