@@ -18,26 +18,28 @@
 //   attn_bwd_dq_kernel    one CTA per SM, persistent over (head, 128-row query block).
 //
 // attn_bwd_dkdv_kernel, 352 threads:
-//   warp 0      TMA producer: K, V once per item; per 128-row query block Q and dO
-//               (2-stage rings; Q's stage also carries its lse and Delta rows by 1-D
-//               bulk copy).
+//   warp 0      TMA producer: K, V once per item; per 128-row query block Q (2-stage
+//               ring; each stage also carries the block's lse and Delta rows by 1-D bulk
+//               copy) and dO (1 stage).
 //   warps 1, 2  MMA issuers (lane 0 of each); warp 1 also owns TMEM:
-//                 warp 1:  dV  += P^T dO   TS  (A = P^T bf16 in TMEM [0,32) + [64,96),
-//                                               B = dO MN-major), then
-//                          S^T  = K Q^T    SS  -> TMEM [0,128)   (A = K, B = Q, K-major)
-//                 warp 2:  dK  += dS^T Q   TS  (A = dS^T bf16 in TMEM [128,160) +
-//                                               [192,224), B = Q MN-major), then
-//                          dP^T = V dO^T   SS  -> TMEM [128,256)
-//               One thread issues at most one MMA per ~93 cycles on this GPU, so two
-//               issuers keep the tensor core busy.  Each stream only overwrites TMEM that
-//               its own earlier MMAs read (S^T over P^T, dP^T over dS^T), so in-order
-//               issue within a stream is all the ordering the TMEM reuse needs; operands
-//               both streams read (Q, dO, K/V) are released by one commit from each.
+//                 warp 1:  S^T_{b+1} = K Q^T  SS  -> TMEM [0,128)   (A = K, B = Q, K-major)
+//                          as soon as the compute warps have read S^T_b, then
+//                          dV  += P^T_b dO    SS  (A = the P^T smem tile, K-major;
+//                                                  B = dO MN-major)
+//                 warp 2:  dK  += dS^T_b Q    TS  (A = dS^T bf16 in TMEM [128,160) +
+//                                                  [192,224), B = Q MN-major), then
+//                          dP^T_{b+1} = V dO^T SS -> TMEM [128,256)
+//               The two streams run side by side.  P^T lives in shared memory, so the next
+//               S^T never waits for dV; dP^T_{b+1} overwrites dS^T_b after dK_b in warp
+//               2's own order.  Operands both streams read (Q, dO, K/V) are released by
+//               one commit from each.
 //   warps 3-10  two compute warpgroups, each owning 64 of a block's 128 query columns:
-//               P phase (P^T from S^T, bf16 over the group's S^T columns), dS phase
-//               (dS^T from dP^T, bf16 over the group's dP^T columns), and per item one of
-//               dV / dK -> bf16 global.
+//               P phase (P^T from S^T, bf16 into the group's chunk of the P^T smem tile),
+//               dS phase (dS^T from dP^T, bf16 over the group's dP^T columns), and per
+//               item one of dV / dK -> bf16 global.
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
+// Shared memory: K, V (one tile each), Q (2 stages), dO (1 stage), the P^T tile (128 keys
+// x 128 queries bf16, two 128-byte-swizzled chunks of 64 queries).
 #include "qat_internal.h"
 #include "qat_quant.cuh"
 #include "sm100.cuh"
@@ -62,8 +64,9 @@ struct BwdTc {
   static constexpr uint32_t kOffK = 0;
   static constexpr uint32_t kOffV = kOffK + kTileBytes;
   static constexpr uint32_t kOffQ = kOffV + kTileBytes;     // 2 stages
-  static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;  // 2 stages
-  static constexpr uint32_t kOffLse = kOffDO + 2 * kTileBytes;   // 2 stages x 512 B
+  static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;  // 1 stage
+  static constexpr uint32_t kOffPT = kOffDO + kTileBytes;     // P^T: 2 chunks of 64 queries
+  static constexpr uint32_t kOffLse = kOffPT + 2 * kChunkBytes;  // 2 stages x 512 B
   static constexpr uint32_t kOffDelta = kOffLse + 1024;          // 2 stages x 512 B
   static constexpr uint32_t kOffPx = kOffDelta + 1024;   // quant_mode 2: tile maxima, scales
   static constexpr uint32_t kOffBar = kOffPx + 8192;
@@ -74,8 +77,8 @@ struct BwdTc {
 };
 
 enum : uint32_t {
-  B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL0,
-  B_DO_FULL1, B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL,
+  B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL,
+  B_DO_EMPTY, B_S_FULL, B_S_EMPTY, B_PT_FREE, B_DP_FULL, B_P_FULL, B_DS_FULL,
   B_DKDV_FULL, B_DKDV_EMPTY, B_DRAIN, B_DRAIN_B, B_PX0, B_PX1, B_PX2, B_PX3, B_COUNT
 };
 
@@ -143,8 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t i = 0; i < B_COUNT; ++i) {
       // released by one commit from each MMA issuer
       const bool both = i == B_KV_EMPTY || i == B_Q_EMPTY0 || i == B_Q_EMPTY1 ||
-                        i == B_DO_EMPTY0 || i == B_DO_EMPTY1 || i == B_DKDV_FULL;
-      const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DKDV_EMPTY)
+                        i == B_DO_EMPTY || i == B_DKDV_FULL;
+      const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DKDV_EMPTY ||
+                            i == B_S_EMPTY)
                                ? 256u : (i >= B_PX0 ? 64u : (both ? 2u : 1u));
       mbar_init(bar(i), cnt);
     }
@@ -198,13 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = load_q(bh, block_at(first, 0, p));
         for (int ii = 0; ii < count && ok; ++ii) {
           const int blk = block_at(first, ii, p);
-          const uint32_t dst = dc & 1, duse = dc >> 1;
-          ok = mbar_wait(bar(B_DO_EMPTY0 + dst), (duse & 1) ^ 1, abort_flag, p.err);
+          ok = mbar_wait(bar(B_DO_EMPTY), (dc & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar(B_DO_FULL0 + dst), C::kTileBytes);
+          mbar_arrive_expect_tx(bar(B_DO_FULL), C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(base + C::kOffDO + dst * C::kTileBytes + c * C::kChunkBytes, &tmDO,
-                        bar(B_DO_FULL0 + dst), 64 * c, blk * kBlk, bh);
+            tma_load_3d(base + C::kOffDO + c * C::kChunkBytes, &tmDO, bar(B_DO_FULL), 64 * c,
+                        blk * kBlk, bh);
           ++dc;
           if (ii + 1 < count) ok = load_q(bh, block_at(first, ii + 1, p));
         }
@@ -213,71 +216,117 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it > 0) mbar_wait(bar(B_KV_FULL), (it - 1) & 1, abort_flag, p.err);
       for (uint32_t i = (qc > 2 ? qc - 2 : 0); i < qc; ++i)
         mbar_wait(bar(B_Q_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
-      for (uint32_t i = (dc > 2 ? dc - 2 : 0); i < dc; ++i)
-        mbar_wait(bar(B_DO_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
+      if (dc > 0) mbar_wait(bar(B_DO_FULL), (dc - 1) & 1, abort_flag, p.err);
     }
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer A: S^T, dV
     if (lane == 0) {
-      const bool ia = warp == 1;  // A: dV, S^T   B: dK, dP^T
-      constexpr uint32_t idSS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T, dP^T
-      constexpr uint32_t idKM = idesc_bf16_f32(kBlk, D, true, false);      // dV, dK
-      // stream A reads K and writes S^T; stream B reads V and writes dP^T
-      const uint32_t sKV = base + (ia ? C::kOffK : C::kOffV);
-      const uint32_t tScore = tbase + (ia ? C::kTmemS : C::kTmemDP);
-      const uint32_t tAcc = tbase + (ia ? C::kTmemDV : C::kTmemDK);
+      constexpr uint32_t idSS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T
+      constexpr uint32_t idKM = idesc_bf16_f32(kBlk, D, true, false);      // dV
+      const uint32_t sK = base + C::kOffK, sDO = base + C::kOffDO, sPT = base + C::kOffPT;
       uint32_t qc = 0;  // query blocks processed (global)
       int it = 0;
       bool ok = true, issued = false;
       auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
-      // the score tile of block c: A: S^T_c = K Q_c^T, B: dP^T_c = V dO_c^T
-      auto issue_score = [&](uint32_t c) -> bool {
+      auto issue_s = [&](uint32_t c) -> bool {  // S^T_c = K Q_c^T
         const uint32_t st = c & 1;
-        if (!w(bar((ia ? B_Q_FULL0 : B_DO_FULL0) + st), (c >> 1) & 1)) return false;
+        if (!w(bar(B_Q_FULL0 + st), (c >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t sB = base + (ia ? C::kOffQ : C::kOffDO) + st * C::kTileBytes;
+        const uint32_t sQ = base + C::kOffQ + st * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tScore, smem_desc_sw128(sKV + off, 16, 1024), smem_desc_sw128(sB + off, 16, 1024),
-                 idSS, ks > 0 ? 1u : 0u);
+          mma_ss(tbase + C::kTmemS, smem_desc_sw128(sK + off, 16, 1024),
+                 smem_desc_sw128(sQ + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(bar(ia ? B_S_FULL : B_DP_FULL));
+        mma_commit(bar(B_S_FULL));
         issued = true;
         return true;
       };
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, kb, first, count;
         bwd_item(idx, p, bh, kb, first, count);
-        ok = w(bar(B_KV_FULL), it & 1) && issue_score(qc);
+        ok = w(bar(B_KV_FULL), it & 1);
+        // S^T overwrites the previous block's S^T once the compute warps have read it
+        if (ok && qc > 0) ok = w(bar(B_S_EMPTY), (qc - 1) & 1);
+        if (ok) ok = issue_s(qc);
         for (int ii = 0; ii < count && ok; ++ii, ++qc) {
-          const uint32_t st = qc & 1;
-          // A: dV += P^T dO (P^T at [0,32) + [64,96));  B: dK += dS^T Q (dS^T at
-          // [128,160) + [192,224)); the B operand is the tile the other stream scored
-          if (!(ok = w(bar(ia ? B_P_FULL : B_DS_FULL), qc & 1))) break;
-          if (!(ok = w(bar((ia ? B_DO_FULL0 : B_Q_FULL0) + st), (qc >> 1) & 1))) break;
+          if (ii + 1 < count && !(ok = w(bar(B_S_EMPTY), qc & 1) && issue_s(qc + 1))) break;
+          // dV += P^T dO, once the compute warps have written P^T of this block
+          if (!(ok = w(bar(B_P_FULL), qc & 1) && w(bar(B_DO_FULL), qc & 1))) break;
           if (ii == 0 && !(ok = w(bar(B_DKDV_EMPTY), (it & 1) ^ 1))) break;
           tc_fence_after();
-          const uint32_t sB = base + (ia ? C::kOffDO : C::kOffQ) + st * C::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks)
-            mma_ts(tAcc, tScore + (ks < 4 ? 8 * ks : 32 + 8 * ks),
-                   smem_desc_sw128(sB + ks * 2048, C::kChunkBytes, 1024), idKM,
+          for (int ks = 0; ks < kBlk / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+            mma_ss(tbase + C::kTmemDV, smem_desc_sw128(sPT + off, 16, 1024),
+                   smem_desc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idKM,
                    (ii > 0 || ks > 0) ? 1u : 0u);
-          // Q_c is read by S^T_c (A) and dK_c (B); dO_c by dP^T_c (B) and dV_c (A): this
-          // stream's last read of either tile of block c is now issued
-          mma_commit(bar(B_Q_EMPTY0 + st));
-          mma_commit(bar(B_DO_EMPTY0 + st));
-          if (ii + 1 < count && !(ok = issue_score(qc + 1))) break;
+          }
+          mma_commit(bar(B_PT_FREE));
+          mma_commit(bar(B_DO_EMPTY));             // dO_c: read by dP^T_c (B) and dV_c
+          mma_commit(bar(B_Q_EMPTY0 + (qc & 1)));  // Q_c: read by S^T_c and dK_c (B)
         }
         if (!ok) break;
         mma_commit(bar(B_KV_EMPTY));
         mma_commit(bar(B_DKDV_FULL));
       }
       if (issued) {
-        const uint32_t dr = bar(ia ? B_DRAIN : B_DRAIN_B);
-        mma_commit(dr);
-        mbar_wait(dr, 0, abort_flag, p.err);
+        mma_commit(bar(B_DRAIN));
+        mbar_wait(bar(B_DRAIN), 0, abort_flag, p.err);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ MMA issuer B: dK, dP^T
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16_f32(kBlk, kBlk, false, false);  // dP^T
+      constexpr uint32_t idKM = idesc_bf16_f32(kBlk, D, true, false);      // dK
+      const uint32_t sV = base + C::kOffV, sDO = base + C::kOffDO;
+      uint32_t qc = 0;
+      int it = 0;
+      bool ok = true, issued = false;
+      auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
+      // dP^T_c = V dO_c^T; it overwrites dS^T_{c-1}, which dK_{c-1} (issued before) reads
+      auto issue_dp = [&](uint32_t c) -> bool {
+        if (!w(bar(B_DO_FULL), c & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          mma_ss(tbase + C::kTmemDP, smem_desc_sw128(sV + off, 16, 1024),
+                 smem_desc_sw128(sDO + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_DP_FULL));
+        mma_commit(bar(B_DO_EMPTY));
+        issued = true;
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
+        int bh, kb, first, count;
+        bwd_item(idx, p, bh, kb, first, count);
+        ok = w(bar(B_KV_FULL), it & 1) && issue_dp(qc);
+        for (int ii = 0; ii < count && ok; ++ii, ++qc) {
+          const uint32_t st = qc & 1;
+          // dK += dS^T Q  (dS^T halves at columns [128,160) and [192,224))
+          if (!(ok = w(bar(B_DS_FULL), qc & 1) && w(bar(B_Q_FULL0 + st), (qc >> 1) & 1))) break;
+          if (ii == 0 && !(ok = w(bar(B_DKDV_EMPTY), (it & 1) ^ 1))) break;
+          tc_fence_after();
+          const uint32_t sQ = base + C::kOffQ + st * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kBlk / 16; ++ks)
+            mma_ts(tbase + C::kTmemDK, tbase + C::kTmemDP + (ks < 4 ? 8 * ks : 32 + 8 * ks),
+                   smem_desc_sw128(sQ + ks * 2048, C::kChunkBytes, 1024), idKM,
+                   (ii > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(B_Q_EMPTY0 + st));
+          if (ii + 1 < count && !(ok = issue_dp(qc + 1))) break;
+        }
+        if (!ok) break;
+        mma_commit(bar(B_KV_EMPTY));
+        mma_commit(bar(B_DKDV_FULL));
+      }
+      if (issued) {
+        mma_commit(bar(B_DRAIN_B));
+        mbar_wait(bar(B_DRAIN_B), 0, abort_flag, p.err);
       }
     }
   } else {
@@ -297,7 +346,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, okw) != 0;
     };
     uint32_t Pp[32];                                  // P^T of the current block, bf16 pairs
-    // P phase of block `blk` (global index c): P^T -> TMEM for the dV MMA
+    // this thread's row of P^T (64 queries of chunk h) into the swizzled smem tile, once
+    // dV of the previous block has read the tile
+    const uint32_t ptrow = base + C::kOffPT + h * C::kChunkBytes + r * 128;
+    const uint32_t sw = static_cast<uint32_t>(r & 7);
+    auto store_pt = [&](uint32_t c, const uint32_t (&v)[32]) -> bool {
+      if (c > 0 && !wwait(bar(B_PT_FREE), (c - 1) & 1)) return false;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ptrow + ((u ^ sw) << 4)),
+                     "r"(v[4 * u]), "r"(v[4 * u + 1]), "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
+                     : "memory");
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_P_FULL));
+      return true;
+    };
+    // P phase of block `blk` (global index c): P^T -> the smem tile for the dV MMA
     auto p_phase = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
       const uint32_t st = c & 1;
       const float* sl = reinterpret_cast<const float*>(gbase + C::kOffLse + st * 512) + 64 * h;
@@ -311,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tbase + lrow + C::kTmemS + 64 * h + 32,
                   *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(B_S_EMPTY));                   // the next S^T may overwrite TMEM S^T
 #pragma unroll
         for (int i = 0; i < 64; i += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
@@ -332,13 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tmem_st16(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<const uint32_t(*)[16]>(&Pp[0]));
-      tmem_st16(tbase + lrow + C::kTmemS + 64 * h + 16,
-                *reinterpret_cast<const uint32_t(*)[16]>(&Pp[16]));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(B_P_FULL));
-      return true;
+      return store_pt(c, Pp);
     };
     // quant_mode 2 (the page's backward, "attn_qat_train.py" _attn_bwd_dkdv): the dV MMA
     // consumes P^T quantized per (query, 64-key tile) with the forward's rule.  The 64
@@ -359,6 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
       tmem_ld32(tbase + lrow + C::kTmemS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_S_EMPTY));
 #pragma unroll
       for (int i = 0; i < 64; i += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
@@ -412,13 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pq[i / 2] = pack_bf16x2(d.x, d.y);
       }
       __syncwarp();                                    // ws is rewritten next block
-      tmem_st16(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<const uint32_t(*)[16]>(&pq[0]));
-      tmem_st16(tbase + lrow + C::kTmemS + 64 * h + 16,
-                *reinterpret_cast<const uint32_t(*)[16]>(&pq[16]));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(B_P_FULL));
-      return true;
+      return store_pt(c, pq);
     };
     // dS phase of block c: dS^T = P^T o (dP^T - Delta) -> bf16 over this group's dP^T
     // columns (each 32-column load is consumed before the 16 packed columns it becomes
