@@ -18,9 +18,9 @@
 //                 dQ += dS K      TS  (A = dS bf16 in TMEM, B = K_j MN-major) -> TMEM dQ
 //   warp 2      lane 0 issues dP = dO V^T (SS, A = dO K-major, B = V_j K-major) -> TMEM dP
 //               as soon as the compute warps have read the previous dP.
-//               One thread issues at most one MMA per ~93 cycles on this GPU, so the
-//               products come from two issuers.  S, dP and dS each have their own TMEM
-//               columns, so no product waits for another block's dQ.
+//               Two issuers let the dP stream run ahead independently of the S / dQ
+//               stream.  S, dP and dS each have their own TMEM columns, so no product
+//               waits for another block's dQ.
 //   warps 3-10  two compute warpgroups; group h owns keys [64h, 64h + 64) of every block,
 //               each thread one query row (TMEM lane): P from S, dS from P and dP into
 //               the dS columns, and at the end half of dQ's columns to global memory.
@@ -105,8 +105,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Bounds of 384 threads cap registers at 168 per thread: with 11 warps, three share a
+// sub-partition's 16K registers, so a 352-thread CTA cannot launch with more.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmDO, const DqParams p) {

@@ -124,8 +124,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Bounds of 384 threads cap registers at 168 per thread: with 11 warps, three share a
+// sub-partition's 16K registers, so a 352-thread CTA cannot launch with more.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,

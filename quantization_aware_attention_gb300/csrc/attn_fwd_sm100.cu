@@ -15,9 +15,9 @@
 //   warp 2      lane 0 issues the value MMAs:
 //                 O_q += Pq_j V_j          (TS: A = Pq in TMEM, B = V MN-major in smem)
 //                 O_hp += P_j V_j          (TS, same V descriptors: the two P tiles share V)
-//               One thread issues at most one MMA per ~93 cycles on this GPU; two issuers
-//               keep the tensor core busy.  S_{j+2} reuses the buffer that holds P_j, so
-//               warp 1 waits for warp 2's commit of PV_j before issuing it.
+//               The two streams progress independently: scores run ahead while the value
+//               MMAs wait for P.  S_{j+2} reuses the buffer that holds P_j, so warp 1
+//               waits for warp 2's commit of PV_j before issuing it.
 //   warps 3-10  softmax + quantization in two warpgroups: warps 3-6 take keys 0-63 and
 //               warps 7-10 keys 64-127 of each S row (one 64-key quantization tile per
 //               thread), exchanging the row max through shared memory.  P is written
@@ -117,8 +117,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Bounds of 384 threads cap registers at 168 per thread: with 11 warps, three share a
+// sub-partition's 16K registers, so a 352-thread CTA cannot launch with more.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const TcParams p) {
