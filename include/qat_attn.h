@@ -95,9 +95,10 @@ QAT_API qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v,
                           void* stream);
 
 /*
- * qat_attn_bwd_workspace_bytes -- device workspace qat_attn_bwd needs for these sizes
- * (fp32 Delta [B, H, Nq] and scratch, 256-byte aligned pieces).  Returns 0 for
- * invalid sizes.  Host-only; never touches the device.
+ * qat_attn_bwd_workspace_bytes -- device workspace qat_attn_bwd needs for these sizes:
+ * fp32 lse and Delta, each [B, H, Nq rounded up to a multiple of 128] in a 256-byte
+ * aligned piece, i.e. about 8 bytes per query row.  Returns 0 for invalid sizes.
+ * Host-only; never touches the device.
  */
 QAT_API size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D);
 

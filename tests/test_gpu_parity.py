@@ -144,15 +144,15 @@ def test_backward_without_queries_zeroes_key_grads():
     assert st == Status.OK and not dk.any() and not dv.any()
 
 
-def test_deterministic():
-    """Forward outputs, dK and dV are bit-identical run to run; dQ is summed over key
-    blocks by reduce-adds in L2 whose order may vary, so it agrees to fp32 rounding."""
+@pytest.mark.parametrize("causal", [False, True])
+def test_deterministic(causal):
+    """Every output is bit-identical run to run: each CTA sums its own rows in a fixed
+    order (dQ per query block in TMEM, dK/dV per key block), with no atomics."""
     inp = custom_inputs(91, 1, 2, 300, 300, 128)
-    a = run_gpu(inp, False, 0.088)
-    b = run_gpu(inp, False, 0.088)
-    for n in ("o_q", "o_hp", "lse", "dk", "dv"):
+    a = run_gpu(inp, causal, 0.088)
+    b = run_gpu(inp, causal, 0.088)
+    for n in ("o_q", "o_hp", "lse", "dq", "dk", "dv"):
         assert torch.equal(a[n], b[n]), n
-    assert rel_l2(host_f64(a["dq"]), host_f64(b["dq"])) < 1e-5
 
 
 # ------------------------------------------------------------------ full-size, sampled
