@@ -18,28 +18,29 @@
 //   attn_bwd_dq_kernel    one CTA per SM, persistent over (head, 128-row query block).
 //
 // attn_bwd_dkdv_kernel, 352 threads:
-//   warp 0      TMA producer: K, V once per item; per 128-row query block Q (2-stage
-//               ring; each stage also carries the block's lse and Delta rows by 1-D bulk
-//               copy) and dO (1 stage).
+//   warp 0      TMA producer: the ones tile once; K, V once per item; per 128-row query
+//               block Q with its lse_ext rows and dO with its d_ext rows (2 stages each).
 //   warps 1, 2  MMA issuers (lane 0 of each); warp 1 also owns TMEM:
-//                 warp 1:  S^T_{b+1} = K Q^T  SS  -> TMEM [0,128)   (A = K, B = Q, K-major)
-//                          as soon as the compute warps have read S^T_b, then
-//                          dV  += P^T_b dO    SS  (A = the P^T smem tile, K-major;
-//                                                  B = dO MN-major)
+//                 warp 1:  dV  += P^T_b dO    TS  (A = P^T bf16 in TMEM [0,32) + [64,96),
+//                                                  B = dO MN-major), then
+//                          S^T_{b+1} = K Q^T  SS  -> TMEM [0,128)   (A = K, B = Q, K-major)
 //                 warp 2:  dK  += dS^T_b Q    TS  (A = dS^T bf16 in TMEM [128,160) +
 //                                                  [192,224), B = Q MN-major), then
 //                          dP^T_{b+1} = V dO^T SS -> TMEM [128,256)
-//               The two streams run side by side.  P^T lives in shared memory, so the next
-//               S^T never waits for dV; dP^T_{b+1} overwrites dS^T_b after dK_b in warp
-//               2's own order.  Operands both streams read (Q, dO, K/V) are released by
-//               one commit from each.
+//               Each score product takes one more k-step: a constant ones tile times the
+//               query block's lse_ext (d_ext) rows, so TMEM receives S^T - lse / qk_scale
+//               and dP^T - Delta and the compute warps read no per-query values at all.
+//               Each stream only overwrites TMEM its own earlier MMAs read (S^T over P^T,
+//               dP^T over dS^T); operands both read (Q, dO, K/V) are released by one
+//               commit from each.  Shared-memory bandwidth bounds the kernel: per 128 x
+//               128 block the MMAs read ~208 KB and TMA writes ~72 KB.
 //   warps 3-10  two compute warpgroups, each owning 64 of a block's 128 query columns:
-//               P phase (P^T from S^T, bf16 into the group's chunk of the P^T smem tile),
-//               dS phase (dS^T from dP^T, bf16 over the group's dP^T columns), and per
-//               item one of dV / dK -> bf16 global.
+//               P phase (P^T = exp2(qk_scale (S^T - lse / qk_scale)), bf16 over the
+//               group's S^T columns), dS phase (dS^T = P^T o (dP^T - Delta), bf16 over the
+//               group's dP^T columns), and per item one of dV / dK -> bf16 global.
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
-// Shared memory: K, V (one tile each), Q (2 stages), dO (1 stage), the P^T tile (128 keys
-// x 128 queries bf16, two 128-byte-swizzled chunks of 64 queries).
+// Shared memory: K, V (one tile each), Q and dO (2 stages each, 128-byte swizzle), the
+// ones tile and the lse_ext / d_ext rows (128 x 16 bf16, 32-byte swizzle).
 #include "qat_internal.h"
 #include "qat_quant.cuh"
 #include "sm100.cuh"
@@ -64,11 +65,12 @@ struct BwdTc {
   static constexpr uint32_t kOffK = 0;
   static constexpr uint32_t kOffV = kOffK + kTileBytes;
   static constexpr uint32_t kOffQ = kOffV + kTileBytes;     // 2 stages
-  static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;  // 1 stage
-  static constexpr uint32_t kOffPT = kOffDO + kTileBytes;     // P^T: 2 chunks of 64 queries
-  static constexpr uint32_t kOffLse = kOffPT + 2 * kChunkBytes;  // 2 stages x 512 B
-  static constexpr uint32_t kOffDelta = kOffLse + 1024;          // 2 stages x 512 B
-  static constexpr uint32_t kOffPx = kOffDelta + 1024;   // quant_mode 2: tile maxima, scales
+  static constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;  // 2 stages
+  static constexpr uint32_t kExtBytes = kBlk * 32;            // 128 rows x 16 bf16 (SW32)
+  static constexpr uint32_t kOffOnes = kOffDO + 2 * kTileBytes;  // ones tile
+  static constexpr uint32_t kOffQX = kOffOnes + kExtBytes;    // lse_ext, 2 stages with Q
+  static constexpr uint32_t kOffDX = kOffQX + 2 * kExtBytes;  // d_ext, 2 stages with dO
+  static constexpr uint32_t kOffPx = kOffDX + 2 * kExtBytes;  // quant_mode 2: tile maxima, scales
   static constexpr uint32_t kOffBar = kOffPx + 8192;
   static constexpr uint32_t kOffMisc = kOffBar + 256;
   static constexpr uint32_t kUsed = kOffMisc + 64;
@@ -77,8 +79,8 @@ struct BwdTc {
 };
 
 enum : uint32_t {
-  B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL,
-  B_DO_EMPTY, B_S_FULL, B_S_EMPTY, B_PT_FREE, B_DP_FULL, B_P_FULL, B_DS_FULL,
+  B_ONES_FULL = 0, B_KV_FULL, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1,
+  B_DO_FULL0, B_DO_FULL1, B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL,
   B_DKDV_FULL, B_DKDV_EMPTY, B_DRAIN, B_DRAIN_B, B_PX0, B_PX1, B_PX2, B_PX3, B_COUNT
 };
 
@@ -131,7 +133,10 @@ __global__ void __launch_bounds__(384, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmDO, const BwdTcParams p) {
+                         const __grid_constant__ CUtensorMap tmDO,
+                         const __grid_constant__ CUtensorMap tmQX,
+                         const __grid_constant__ CUtensorMap tmDX,
+                         const __grid_constant__ CUtensorMap tmOnes, const BwdTcParams p) {
   using C = BwdTc<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -148,9 +153,8 @@ __global__ void __launch_bounds__(384, 1)
     for (uint32_t i = 0; i < B_COUNT; ++i) {
       // released by one commit from each MMA issuer
       const bool both = i == B_KV_EMPTY || i == B_Q_EMPTY0 || i == B_Q_EMPTY1 ||
-                        i == B_DO_EMPTY || i == B_DKDV_FULL;
-      const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DKDV_EMPTY ||
-                            i == B_S_EMPTY)
+                        i == B_DO_EMPTY0 || i == B_DO_EMPTY1 || i == B_DKDV_FULL;
+      const uint32_t cnt = (i == B_P_FULL || i == B_DS_FULL || i == B_DKDV_EMPTY)
                                ? 256u : (i >= B_PX0 ? 64u : (both ? 2u : 1u));
       mbar_init(bar(i), cnt);
     }
@@ -159,6 +163,9 @@ __global__ void __launch_bounds__(384, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    prefetch_tmap(&tmQX);
+    prefetch_tmap(&tmDX);
+    prefetch_tmap(&tmOnes);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
@@ -175,17 +182,19 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t qc = 0, dc = 0;  // Q loads, dO loads issued
       int it = 0;
       bool ok = true;
+      // the ones tile, once per CTA
+      mbar_arrive_expect_tx(bar(B_ONES_FULL), C::kExtBytes);
+      tma_load_3d(base + C::kOffOnes, &tmOnes, bar(B_ONES_FULL), 0, 0, 0);
+      // Q_blk with its lse_ext rows
       auto load_q = [&](int bh, int blk) -> bool {
         const uint32_t st = qc & 1, use = qc >> 1;
         if (!mbar_wait(bar(B_Q_EMPTY0 + st), (use & 1) ^ 1, abort_flag, p.err)) return false;
         const uint32_t fb = bar(B_Q_FULL0 + st);
-        mbar_arrive_expect_tx(fb, C::kTileBytes + 1024);
+        mbar_arrive_expect_tx(fb, C::kTileBytes + C::kExtBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(base + C::kOffQ + st * C::kTileBytes + c * C::kChunkBytes, &tmQ, fb, 64 * c,
                       blk * kBlk, bh);
-        const size_t row0 = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(blk) * kBlk;
-        bulk_load(base + C::kOffLse + st * 512, p.a.lse_pad + row0, 512, fb);
-        bulk_load(base + C::kOffDelta + st * 512, p.a.delta + row0, 512, fb);
+        tma_load_3d(base + C::kOffQX + st * C::kExtBytes, &tmQX, fb, 0, blk * kBlk, bh);
         ++qc;
         return true;
       };
@@ -204,12 +213,15 @@ __global__ void __launch_bounds__(384, 1)
         ok = load_q(bh, block_at(first, 0, p));
         for (int ii = 0; ii < count && ok; ++ii) {
           const int blk = block_at(first, ii, p);
-          ok = mbar_wait(bar(B_DO_EMPTY), (dc & 1) ^ 1, abort_flag, p.err);
+          const uint32_t dst = dc & 1, duse = dc >> 1;
+          ok = mbar_wait(bar(B_DO_EMPTY0 + dst), (duse & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar(B_DO_FULL), C::kTileBytes);
+          const uint32_t fb = bar(B_DO_FULL0 + dst);
+          mbar_arrive_expect_tx(fb, C::kTileBytes + C::kExtBytes);
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(base + C::kOffDO + c * C::kChunkBytes, &tmDO, bar(B_DO_FULL), 64 * c,
-                        blk * kBlk, bh);
+            tma_load_3d(base + C::kOffDO + dst * C::kTileBytes + c * C::kChunkBytes, &tmDO, fb,
+                        64 * c, blk * kBlk, bh);
+          tma_load_3d(base + C::kOffDX + dst * C::kExtBytes, &tmDX, fb, 0, blk * kBlk, bh);
           ++dc;
           if (ii + 1 < count) ok = load_q(bh, block_at(first, ii + 1, p));
         }
@@ -218,14 +230,16 @@ __global__ void __launch_bounds__(384, 1)
       if (it > 0) mbar_wait(bar(B_KV_FULL), (it - 1) & 1, abort_flag, p.err);
       for (uint32_t i = (qc > 2 ? qc - 2 : 0); i < qc; ++i)
         mbar_wait(bar(B_Q_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
-      if (dc > 0) mbar_wait(bar(B_DO_FULL), (dc - 1) & 1, abort_flag, p.err);
+      for (uint32_t i = (dc > 2 ? dc - 2 : 0); i < dc; ++i)
+        mbar_wait(bar(B_DO_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
+      mbar_wait(bar(B_ONES_FULL), 0, abort_flag, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer A: S^T, dV
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(kBlk, kBlk, false, false);  // S^T
       constexpr uint32_t idKM = idesc_bf16_f32(kBlk, D, true, false);      // dV
-      const uint32_t sK = base + C::kOffK, sDO = base + C::kOffDO, sPT = base + C::kOffPT;
+      const uint32_t sK = base + C::kOffK;
       uint32_t qc = 0;  // query blocks processed (global)
       int it = 0;
       bool ok = true, issued = false;
@@ -241,33 +255,35 @@ __global__ void __launch_bounds__(384, 1)
           mma_ss(tbase + C::kTmemS, smem_desc_sw128(sK + off, 16, 1024),
                  smem_desc_sw128(sQ + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
         }
+        // one more k-step: ones x lse_ext adds -lse / qk_scale to every key row
+        mma_ss(tbase + C::kTmemS, smem_desc_sw32(base + C::kOffOnes),
+               smem_desc_sw32(base + C::kOffQX + st * C::kExtBytes), idSS, 1u);
         mma_commit(bar(B_S_FULL));
         issued = true;
         return true;
       };
+      ok = w(bar(B_ONES_FULL), 0);
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, kb, first, count;
         bwd_item(idx, p, bh, kb, first, count);
-        ok = w(bar(B_KV_FULL), it & 1);
-        // S^T overwrites the previous block's S^T once the compute warps have read it
-        if (ok && qc > 0) ok = w(bar(B_S_EMPTY), (qc - 1) & 1);
-        if (ok) ok = issue_s(qc);
+        ok = w(bar(B_KV_FULL), it & 1) && issue_s(qc);
         for (int ii = 0; ii < count && ok; ++ii, ++qc) {
-          if (ii + 1 < count && !(ok = w(bar(B_S_EMPTY), qc & 1) && issue_s(qc + 1))) break;
-          // dV += P^T dO, once the compute warps have written P^T of this block
-          if (!(ok = w(bar(B_P_FULL), qc & 1) && w(bar(B_DO_FULL), qc & 1))) break;
+          const uint32_t dst = qc & 1;
+          // dV += P^T dO (TS: P^T halves at TMEM columns [0,32) and [64,96)), once the
+          // compute warps have written P^T of this block over its S^T
+          if (!(ok = w(bar(B_P_FULL), qc & 1) && w(bar(B_DO_FULL0 + dst), (qc >> 1) & 1))) break;
           if (ii == 0 && !(ok = w(bar(B_DKDV_EMPTY), (it & 1) ^ 1))) break;
           tc_fence_after();
+          const uint32_t sDO = base + C::kOffDO + dst * C::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-            mma_ss(tbase + C::kTmemDV, smem_desc_sw128(sPT + off, 16, 1024),
+          for (int ks = 0; ks < kBlk / 16; ++ks)
+            mma_ts(tbase + C::kTmemDV, tbase + C::kTmemS + (ks < 4 ? 8 * ks : 32 + 8 * ks),
                    smem_desc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idKM,
                    (ii > 0 || ks > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(B_PT_FREE));
-          mma_commit(bar(B_DO_EMPTY));             // dO_c: read by dP^T_c (B) and dV_c
+          mma_commit(bar(B_DO_EMPTY0 + dst));     // dO_c: read by dP^T_c (B) and dV_c
           mma_commit(bar(B_Q_EMPTY0 + (qc & 1)));  // Q_c: read by S^T_c and dK_c (B)
+          // S^T_{c+1} overwrites P^T_c after dV_c, in this stream's order
+          if (ii + 1 < count && !(ok = issue_s(qc + 1))) break;
         }
         if (!ok) break;
         mma_commit(bar(B_KV_EMPTY));
@@ -283,26 +299,31 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(kBlk, kBlk, false, false);  // dP^T
       constexpr uint32_t idKM = idesc_bf16_f32(kBlk, D, true, false);      // dK
-      const uint32_t sV = base + C::kOffV, sDO = base + C::kOffDO;
+      const uint32_t sV = base + C::kOffV;
       uint32_t qc = 0;
       int it = 0;
       bool ok = true, issued = false;
       auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
       // dP^T_c = V dO_c^T; it overwrites dS^T_{c-1}, which dK_{c-1} (issued before) reads
       auto issue_dp = [&](uint32_t c) -> bool {
-        if (!w(bar(B_DO_FULL), c & 1)) return false;
+        if (!w(bar(B_DO_FULL0 + (c & 1)), (c >> 1) & 1)) return false;
         tc_fence_after();
+        const uint32_t sDO = base + C::kOffDO + (c & 1) * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
           mma_ss(tbase + C::kTmemDP, smem_desc_sw128(sV + off, 16, 1024),
                  smem_desc_sw128(sDO + off, 16, 1024), idSS, ks > 0 ? 1u : 0u);
         }
+        // one more k-step: ones x d_ext subtracts Delta from every key row
+        mma_ss(tbase + C::kTmemDP, smem_desc_sw32(base + C::kOffOnes),
+               smem_desc_sw32(base + C::kOffDX + (c & 1) * C::kExtBytes), idSS, 1u);
         mma_commit(bar(B_DP_FULL));
-        mma_commit(bar(B_DO_EMPTY));
+        mma_commit(bar(B_DO_EMPTY0 + (c & 1)));
         issued = true;
         return true;
       };
+      ok = w(bar(B_ONES_FULL), 0);
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, kb, first, count;
         bwd_item(idx, p, bh, kb, first, count);
@@ -348,26 +369,22 @@ __global__ void __launch_bounds__(384, 1)
       return __all_sync(0xffffffffu, okw) != 0;
     };
     uint32_t Pp[32];                                  // P^T of the current block, bf16 pairs
-    // this thread's row of P^T (64 queries of chunk h) into the swizzled smem tile, once
-    // dV of the previous block has read the tile
-    const uint32_t ptrow = base + C::kOffPT + h * C::kChunkBytes + r * 128;
-    const uint32_t sw = static_cast<uint32_t>(r & 7);
-    auto store_pt = [&](uint32_t c, const uint32_t (&v)[32]) -> bool {
-      if (c > 0 && !wwait(bar(B_PT_FREE), (c - 1) & 1)) return false;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ptrow + ((u ^ sw) << 4)),
-                     "r"(v[4 * u]), "r"(v[4 * u + 1]), "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
-                     : "memory");
-      fence_proxy_async_smem();
+    // this thread's row of P^T (64 queries, bf16 pairs) over its S^T columns [64h, 64h+32):
+    // the A operand of the dV MMA
+    auto store_pt = [&](const uint32_t (&v)[32]) -> bool {
+      tmem_st16(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<const uint32_t(*)[16]>(&v[0]));
+      tmem_st16(tbase + lrow + C::kTmemS + 64 * h + 16,
+                *reinterpret_cast<const uint32_t(*)[16]>(&v[16]));
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(bar(B_P_FULL));
       return true;
     };
-    // P phase of block `blk` (global index c): P^T -> the smem tile for the dV MMA
+    // P phase of block `blk` (global index c): P^T -> TMEM for the dV MMA
     auto p_phase = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
       const uint32_t st = c & 1;
-      const float* sl = reinterpret_cast<const float*>(gbase + C::kOffLse + st * 512) + 64 * h;
-      if (!(wwait(bar(B_Q_FULL0 + st), (c >> 1) & 1) && wwait(bar(B_S_FULL), c & 1))) return false;
+      (void)st;
+      if (!wwait(bar(B_S_FULL), c & 1)) return false;
       tc_fence_after();
       const bool diag = p.a.causal && blk == kb;
       const int qh = blk * kBlk + 64 * h;             // first query of this thread's columns
@@ -377,17 +394,11 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tbase + lrow + C::kTmemS + 64 * h + 32,
                   *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_S_EMPTY));                   // the next S^T may overwrite TMEM S^T
 #pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
-          const float2 x0 = fma_rn_f32x2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])),
-                                         make_float2(qk, qk), make_float2(-l4.x, -l4.y));
-          const float2 x1 = fma_rn_f32x2(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])),
-                                         make_float2(qk, qk), make_float2(-l4.z, -l4.w));
-          Pp[i / 2] = pack_bf16x2(ex2f(x0.x), ex2f(x0.y));
-          Pp[i / 2 + 1] = pack_bf16x2(ex2f(x1.x), ex2f(x1.y));
+        for (int i = 0; i < 64; i += 2) {           // TMEM holds S^T - lse / qk_scale
+          const float2 x = mul_rn_f32x2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])),
+                                        make_float2(qk, qk));
+          Pp[i / 2] = pack_bf16x2(ex2f(x.x), ex2f(x.y));
         }
         // keys past Nkv (whole rows) and queries before the key on the causal diagonal
         // get P = 0; a separate pass, taken only by the few rows and blocks that need it
@@ -400,7 +411,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      return store_pt(c, Pp);
+      return store_pt(Pp);
     };
     // quant_mode 2 (the page's backward, "attn_qat_train.py" _attn_bwd_dkdv): the dV MMA
     // consumes P^T quantized per (query, 64-key tile) with the forward's rule.  The 64
@@ -412,8 +423,8 @@ __global__ void __launch_bounds__(384, 1)
     const int wip = quarter & 1;
     auto p_phase_page = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
       const uint32_t st = c & 1;
-      const float* sl = reinterpret_cast<const float*>(gbase + C::kOffLse + st * 512) + 64 * h;
-      if (!(wwait(bar(B_Q_FULL0 + st), (c >> 1) & 1) && wwait(bar(B_S_FULL), c & 1))) return false;
+      (void)st;
+      if (!wwait(bar(B_S_FULL), c & 1)) return false;
       tc_fence_after();
       const bool diag = p.a.causal && blk == kb;
       const int qh = blk * kBlk + 64 * h;
@@ -421,19 +432,12 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tbase + lrow + C::kTmemS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
       tmem_ld32(tbase + lrow + C::kTmemS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(B_S_EMPTY));
 #pragma unroll
-      for (int i = 0; i < 64; i += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(sl + i);
-        const float2 x0 = fma_rn_f32x2(make_float2(__uint_as_float(pf[i]), __uint_as_float(pf[i + 1])),
-                                       make_float2(qk, qk), make_float2(-l4.x, -l4.y));
-        const float2 x1 = fma_rn_f32x2(make_float2(__uint_as_float(pf[i + 2]), __uint_as_float(pf[i + 3])),
-                                       make_float2(qk, qk), make_float2(-l4.z, -l4.w));
-        pf[i] = __float_as_uint(ex2f(x0.x));
-        pf[i + 1] = __float_as_uint(ex2f(x0.y));
-        pf[i + 2] = __float_as_uint(ex2f(x1.x));
-        pf[i + 3] = __float_as_uint(ex2f(x1.y));
+      for (int i = 0; i < 64; i += 2) {             // TMEM holds S^T - lse / qk_scale
+        const float2 x = mul_rn_f32x2(make_float2(__uint_as_float(pf[i]), __uint_as_float(pf[i + 1])),
+                                      make_float2(qk, qk));
+        pf[i] = __float_as_uint(ex2f(x.x));
+        pf[i + 1] = __float_as_uint(ex2f(x.y));
       }
       if (__any_sync(0xffffffffu, !key_ok) || diag) {
 #pragma unroll
@@ -476,14 +480,12 @@ __global__ void __launch_bounds__(384, 1)
         pq[i / 2] = pack_bf16x2(d.x, d.y);
       }
       __syncwarp();                                    // ws is rewritten next block
-      return store_pt(c, pq);
+      return store_pt(pq);
     };
     // dS phase of block c: dS^T = P^T o (dP^T - Delta) -> bf16 over this group's dP^T
     // columns (each 32-column load is consumed before the 16 packed columns it becomes
     // are written; dP^T_{c+1} overwrites them only after dK_c has read them)
     auto ds_phase = [&](uint32_t c) -> bool {
-      const float* sd =
-          reinterpret_cast<const float*>(gbase + C::kOffDelta + (c & 1) * 512) + 64 * h;
       if (!wwait(bar(B_DP_FULL), c & 1)) return false;
       tc_fence_after();
 #pragma unroll
@@ -493,17 +495,12 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(sd + 32 * cc + i);
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          const uint32_t pa = Pp[16 * cc + i / 2], pb = Pp[16 * cc + i / 2 + 1];
-          const float pvv[4] = {__uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u),
-                                __uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)};
-          float ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) ds[e] = pvv[e] * (__uint_as_float(dr[i + e]) - dv[e]);
-          pk[i / 2] = pack_bf16x2(ds[0], ds[1]);
-          pk[i / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+        for (int i = 0; i < 32; i += 2) {           // TMEM holds dP^T - Delta
+          const uint32_t pa = Pp[16 * cc + i / 2];
+          const float2 d = mul_rn_f32x2(
+              make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u)),
+              make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])));
+          pk[i / 2] = pack_bf16x2(d.x, d.y);
         }
         tmem_st16(tbase + lrow + C::kTmemDP + 64 * h + 16 * cc, pk);
       }
@@ -568,9 +565,25 @@ __global__ void __launch_bounds__(384, 1)
 
 // ------------------------------------------------------------------ small kernels
 
-// One warp per padded query row: Delta and the lse copy (+inf in padding rows).
+// x as the sum of three bf16 terms (exact to about 2^-27 relative): each term rounds
+// what the previous ones left, and each difference is exact in fp32.
+__device__ __forceinline__ void bf16_split3(float x, uint16_t (&t)[3]) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    t[i] = *reinterpret_cast<const uint16_t*>(&b);
+    x = x - __bfloat162float(b);
+  }
+}
+
+// One warp per padded query row: Delta, the lse copy (+inf in padding rows), and the
+// row's lse_ext / d_ext entries (-lse / qk_scale and -Delta as three bf16 terms; padding
+// rows get -1e30 and 0, so P = 0 there).  Block 0 also writes the ones tile.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x)
+      a.ones[i] = (i & 15) < 3 ? 0x3F80u : 0u;   // bf16 1.0 in elements 0-2
   constexpr int PER = D / 32;
   const long long rows = static_cast<long long>(a.B) * a.H * nq_pad;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -583,6 +596,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
       if (lane == 0) {
         a.delta[rw] = 0.f;
         a.lse_pad[rw] = INFINITY;
+      }
+      if (lane < 16) {
+        uint16_t t[3];
+        bf16_split3(-1e30f, t);
+        a.lse_ext[rw * 16 + lane] = lane == 0 ? t[0] : lane == 1 ? t[1] : lane == 2 ? t[2] : 0u;
+        a.d_ext[rw * 16 + lane] = 0u;
       }
       continue;
     }
@@ -609,9 +628,17 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const float lse = a.lse[bh * a.Nq + q];
     if (lane == 0) {
       a.delta[rw] = acc;
-      a.lse_pad[rw] = a.lse[bh * a.Nq + q];
+      a.lse_pad[rw] = lse;
+    }
+    if (lane < 16) {                                 // every lane holds the full sum
+      uint16_t tl[3], td[3];
+      bf16_split3(-lse / a.qk_scale, tl);
+      bf16_split3(-acc, td);
+      a.lse_ext[rw * 16 + lane] = lane == 0 ? tl[0] : lane == 1 ? tl[1] : lane == 2 ? tl[2] : 0u;
+      a.d_ext[rw * 16 + lane] = lane == 0 ? td[0] : lane == 1 ? td[1] : lane == 2 ? td[2] : 0u;
     }
   }
 }
@@ -635,15 +662,17 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mqx, mdx, mones;
   if (!make_bf16_map_3d(&mq, a.q, D, a.Nq, BH) || !make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) ||
-      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) || !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH))
+      !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) || !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH) ||
+      !make_ext_map_3d(&mqx, a.lse_ext, p.nq_pad, BH) ||
+      !make_ext_map_3d(&mdx, a.d_ext, p.nq_pad, BH) || !make_ext_map_3d(&mones, a.ones, 128, 1))
     return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = p.items < num_sms ? p.items : num_sms;
-  attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, p);
+  attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, mqx, mdx, mones, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_bwd_dq(a, err, num_sms, s);

@@ -536,6 +536,18 @@ bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_ext_map_3d(CUtensorMap* m, const void* ptr, int N, int BH) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {32, static_cast<cuuint64_t>(N) * 32};
+  const cuuint32_t box[3] = {16, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_fwd_tc(const FwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
   return a.D == 64 ? launch_fwd_tc_d<64>(a, err, num_sms, s)
                    : launch_fwd_tc_d<128>(a, err, num_sms, s);

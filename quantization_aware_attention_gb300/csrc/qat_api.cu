@@ -252,6 +252,9 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.dv = static_cast<uint16_t*>(dv);
   a.lse_pad = reinterpret_cast<float*>(ws + wl.off_lse);
   a.delta = reinterpret_cast<float*>(ws + wl.off_delta);
+  a.lse_ext = reinterpret_cast<uint16_t*>(ws + wl.off_lse_ext);
+  a.d_ext = reinterpret_cast<uint16_t*>(ws + wl.off_d_ext);
+  a.ones = reinterpret_cast<uint16_t*>(ws + wl.off_ones);
   a.B = B; a.H = H; a.Nq = Nq; a.Nkv = Nkv; a.D = D;
   a.sm_scale = sm_scale;
   a.qk_scale = sm_scale * kLog2e;

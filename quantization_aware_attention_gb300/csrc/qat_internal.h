@@ -8,10 +8,16 @@
 
 namespace qat {
 
-// Backward workspace: [lse_pad | delta], each piece 256-byte aligned; query rows are
-// padded per head to a multiple of 128.
+// Backward workspace, each piece 256-byte aligned; query rows are padded per head to a
+// multiple of 128:
+//   lse_pad, delta   fp32 [B, H, Nq_pad]
+//   lse_ext, d_ext   bf16 [B, H, Nq_pad, 16]: -lse / qk_scale and -Delta of each row as
+//                    the exact sum of three bf16 terms (elements 0-2, the rest zero)
+//   ones             bf16 [128, 16]: 1 in elements 0-2 of every row
+// The dK/dV kernel multiplies ones by lse_ext (d_ext) in one extra MMA k-step, so its
+// score accumulators come out as S^T - lse / qk_scale and dP^T - Delta.
 struct BwdWorkspace {
-  size_t nq_pad, off_lse, off_delta, total;
+  size_t nq_pad, off_lse, off_delta, off_lse_ext, off_d_ext, off_ones, total;
 };
 
 inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq) {
@@ -21,7 +27,10 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq) {
   const size_t rows_pad = static_cast<size_t>(B) * H * w.nq_pad;
   w.off_lse = 0;
   w.off_delta = up(rows_pad * sizeof(float));
-  w.total = w.off_delta + up(rows_pad * sizeof(float));
+  w.off_lse_ext = w.off_delta + up(rows_pad * sizeof(float));
+  w.off_d_ext = w.off_lse_ext + up(rows_pad * 32);
+  w.off_ones = w.off_d_ext + up(rows_pad * 32);
+  w.total = w.off_ones + up(128 * 32);
   if (w.total == 0) w.total = 256;
   return w;
 }
@@ -30,6 +39,8 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq) {
 // 128-byte swizzle, zero fill out of bounds.
 bool make_bf16_map_3d(CUtensorMap* m, const void* ptr, int D, int N, int BH,
                       int head_rows = -1);
+// [BH, N, 16] bf16 as a 3-D TMA tensor with 16 x 128 x 1 boxes, 32-byte swizzle.
+bool make_ext_map_3d(CUtensorMap* m, const void* ptr, int N, int BH);
 
 // Arguments of one forward launch (device pointers, validated by the ABI layer).
 struct FwdArgs {
@@ -62,6 +73,9 @@ struct BwdArgs {
   uint16_t* dv;
   float* delta;     // fp32 [B, H, Nq_pad] in the workspace (0 in padding rows)
   float* lse_pad;   // fp32 [B, H, Nq_pad] copy of lse (+inf in padding rows)
+  uint16_t* lse_ext;  // bf16 [B, H, Nq_pad, 16] (see BwdWorkspace)
+  uint16_t* d_ext;    // bf16 [B, H, Nq_pad, 16]
+  uint16_t* ones;     // bf16 [128, 16]
   int B, H, Nq, Nkv, D;
   float sm_scale;
   float qk_scale;

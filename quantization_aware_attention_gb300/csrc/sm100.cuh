@@ -258,6 +258,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same descriptor for a K-major operand 16 bf16 (32 bytes) wide in the 32-byte
+// swizzle layout that TMA's SWIZZLE_32B writes: 8-row groups of 256 bytes (SBO), one
+// 16-element k-step per row (LBO unused), swizzle mode 6.
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(256u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(6u) << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator:
 // D format bits 4-5 = 1 (f32), A format bits 7-9 = 1 (bf16), B format bits 10-12 = 1,
 // A major bit 15 (0 = K-major), B major bit 16 (1 = MN-major), N >> 3 in bits 17-22,
