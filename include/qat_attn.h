@@ -95,9 +95,12 @@ QAT_API qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v,
                           void* stream);
 
 /*
- * qat_attn_bwd_workspace_bytes -- device workspace qat_attn_bwd needs for these sizes:
- * fp32 lse and Delta, each [B, H, Nq rounded up to a multiple of 128] in a 256-byte
- * aligned piece, i.e. about 8 bytes per query row.  Returns 0 for invalid sizes.
+ * qat_attn_bwd_workspace_bytes -- device workspace qat_attn_bwd needs for these sizes,
+ * with Nq rounded up to a multiple of 128 per head (Nq_pad), each piece 256-byte
+ * aligned: fp32 lse and Delta [B, H, Nq_pad]; bf16 [B, H, Nq_pad, 16] rows holding
+ * -lse / (sm_scale log2 e) and -Delta, each as a sum of three bf16 terms, which the
+ * dK/dV kernel adds to its score products through one extra MMA step; and a 4 KB
+ * bf16 ones tile.  About 72 bytes per padded query row.  Returns 0 for invalid sizes.
  * Host-only; never touches the device.
  */
 QAT_API size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D);
