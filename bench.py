@@ -471,6 +471,7 @@ def run_ours(args, w):
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     bwd_tf = 10.0 * pairs * D / (bwd_ms * 1e-3) / 1e12
     fwd_tf = 6.0 * pairs * D / (fwd_ms * 1e-3) / 1e12
+    bwd_exec_flops = 14.0 * pairs * D + 2 * 2.0 * pairs * 16
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -493,6 +494,11 @@ def run_ours(args, w):
             "traffic_unit": "bytes per qat_attn_bwd call: its dK/dV and dQ kernels (DRAM read + write)",
             "peak_kind": f"bf16_tflops_sustained ({peak_src})",
             "algorithmic_flops_per_launch": 10.0 * pairs * D,
+            # what the tensor cores execute: S and dP in both kernels (7 products) and the
+            # two K=16 lse / Delta steps of the dK/dV kernel
+            "executed_flops_per_launch": bwd_exec_flops,
+            "executed_achieved": bwd_exec_flops / (bwd_ms * 1e-3) / 1e12,
+            "executed_frac": bwd_exec_flops / (bwd_ms * 1e-3) / 1e12 / peak_sus,
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
