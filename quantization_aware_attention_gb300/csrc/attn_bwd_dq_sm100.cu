@@ -42,8 +42,8 @@ using namespace sm100;
 
 constexpr int kBlk = 128;       // queries per item, keys per block
 constexpr int kThreads = 352;
-constexpr int kKStages = 3;
-constexpr int kVStages = 3;
+constexpr int kKStages = 4;  // K_j stays until dQ_j, issued a block after S_{j+1}
+constexpr int kVStages = 2;
 
 template <int D>
 struct BwdDq {
@@ -216,27 +216,37 @@ __global__ void __launch_bounds__(384, 1)
         if (last) mma_commit(bar(Q_QR_EMPTY));  // the item's last read of its Q rows
         return true;
       };
+      // dQ += dS_c K_c (K tile k), once the compute warps have written dS_c
+      auto issue_dq = [&](uint32_t k, uint32_t c, bool first, bool last) -> bool {
+        if (!w(bar(Q_DS_FULL), c & 1)) return false;
+        if (first && it > 0 && !w(bar(Q_DQ_EMPTY), (it - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t st = k % kKStages;
+        const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBlk / 16; ++ks)
+          mma_ts(tbase + C::kTmemDQ, tbase + C::kTmemDS + 8 * ks,
+                 smem_desc_sw128(sk + ks * 2048, C::kChunkBytes, 1024), idQ,
+                 (!first || ks > 0) ? 1u : 0u);
+        mma_commit(bar(Q_K_EMPTY + st));  // K_c: read by S_c and dQ_c, both issued here
+        mma_commit(bar(Q_DS_FREE));
+        if (last) mma_commit(bar(Q_DQ_FULL));
+        return true;
+      };
+      // Per item: S_0, then for each block j: S_{j+1} and dQ_{j-1}; dQ_{J-1} at the end.
+      // The compute warps write dS_{j-1} only after computing P_j, so dQ lags S by two
+      // blocks and its completion overlaps a whole block of their work.
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, mt, J;
         dq_item(idx, p, bh, mt, J);
         ok = w(bar(Q_QR_FULL), it & 1) && issue_s(kc, bc, J == 1);
-        for (int j = 0; j < J && ok; ++j, ++kc, ++bc) {
-          if (j + 1 < J && !(ok = issue_s(kc + 1, bc + 1, j + 2 == J))) break;
-          // dQ += dS_j K_j, once the compute warps have written dS_j
-          if (!(ok = w(bar(Q_DS_FULL), bc & 1))) break;
-          if (j == 0 && it > 0 && !(ok = w(bar(Q_DQ_EMPTY), (it - 1) & 1))) break;
-          tc_fence_after();
-          const uint32_t st = kc % kKStages;
-          const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks)
-            mma_ts(tbase + C::kTmemDQ, tbase + C::kTmemDS + 8 * ks,
-                   smem_desc_sw128(sk + ks * 2048, C::kChunkBytes, 1024), idQ,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(Q_K_EMPTY + st));  // K_j: read by S_j and dQ_j, both issued here
-          mma_commit(bar(Q_DS_FREE));
-          if (j + 1 == J) mma_commit(bar(Q_DQ_FULL));
+        for (int j = 0; j < J && ok; ++j) {
+          if (j + 1 < J && !(ok = issue_s(kc + j + 1, bc + j + 1, j + 2 == J))) break;
+          if (j >= 1 && !(ok = issue_dq(kc + j - 1, bc + j - 1, j == 1, false))) break;
         }
+        if (ok) ok = issue_dq(kc + J - 1, bc + J - 1, J == 1, true);
+        kc += J;
+        bc += J;
       }
       if (issued) {
         mma_commit(bar(Q_DRAIN_A));
@@ -331,6 +341,19 @@ __global__ void __launch_bounds__(384, 1)
       const size_t prow = static_cast<size_t>(bh) * p.nq_pad + row;
       const float lse_r = p.a.lse_pad[prow];
       const float delta_r = p.a.delta[prow];
+      // dS of block c (keys [64h, 64h + 64)) -> TMEM dS columns [32h, 32h + 32), once dQ
+      // of block c - 1 has read the buffer.  dS_c is held in registers and written after
+      // P of block c + 1 has been computed, so dQ_{c-1} has a block's time to complete.
+      uint32_t pk[32];
+      auto write_ds = [&](uint32_t c) -> bool {
+        if (c > 0 && !wwait(bar(Q_DS_FREE), (c - 1) & 1)) return false;
+        tc_fence_after();
+        tmem_st32(tbase + lrow + C::kTmemDS + 32 * h, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(Q_DS_FULL));
+        return true;
+      };
       for (int j = 0; j < J && ok; ++j, ++bc) {
         if (!(ok = wwait(bar(Q_S_FULL), bc & 1))) break;
         tc_fence_after();
@@ -357,9 +380,9 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 64; ++i)
             if (key0 + i > lim) pr[i] = 0u;
         }
+        if (j > 0 && !(ok = write_ds(bc - 1))) break;
         if (!(ok = wwait(bar(Q_DP_FULL), bc & 1))) break;
         tc_fence_after();
-        uint32_t pk[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t dr[32];
@@ -378,15 +401,8 @@ __global__ void __launch_bounds__(384, 1)
             pk[16 * cc + i] = pack_bf16x2(d.x, d.y);
           }
         }
-        // dS of keys [64h, 64h + 64) -> TMEM dS columns [32h, 32h + 32), once dQ of the
-        // previous block has read the buffer
-        if (bc > 0 && !(ok = wwait(bar(Q_DS_FREE), (bc - 1) & 1))) break;
-        tc_fence_after();
-        tmem_st32(tbase + lrow + C::kTmemDS + 32 * h, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(Q_DS_FULL));
       }
+      if (ok) ok = write_ds(bc - 1);   // the item's last dS
       if (!ok) break;
       // the next item's Q rows go in once this item's last S has read the current ones
       const int nidx = idx + static_cast<int>(gridDim.x);
