@@ -11,9 +11,9 @@
 // passes the gradient of O_q through the quantizer as the identity.
 //
 // CTA layout (352 threads, one CTA per SM, persistent over (head, 128-row query block)):
-//   warp 0      TMA producer: the item's dO tile, then K_j and V_j (3-stage rings each),
-//               128 rows x D in 128-byte-swizzled boxes.
-//   warp 1      TMEM owner; lane 0 issues, in this order, S_{j+1} then dQ_j:
+//   warp 0      TMA producer: the item's dO tile, then K_j (4-stage ring) and V_j
+//               (2-stage ring), 128 rows x D in 128-byte-swizzled boxes.
+//   warp 1      TMEM owner; lane 0 issues, per block j, S_{j+1} then dQ_{j-1}:
 //                 S  = Q K^T      TS  (A = Q bf16 in TMEM, B = K_j K-major)   -> TMEM S
 //                 dQ += dS K      TS  (A = dS bf16 in TMEM, B = K_j MN-major) -> TMEM dQ
 //   warp 2      lane 0 issues dP = dO V^T (SS, A = dO K-major, B = V_j K-major) -> TMEM dP
@@ -22,9 +22,10 @@
 //               stream.  S, dP and dS each have their own TMEM columns, so no product
 //               waits for another block's dQ.
 //   warps 3-10  two compute warpgroups; group h owns keys [64h, 64h + 64) of every block,
-//               each thread one query row (TMEM lane): P from S, dS from P and dP into
-//               the dS columns, and at the end half of dQ's columns to global memory.
-//               Per item they also copy their half of each Q row into TMEM.
+//               each thread one query row (TMEM lane): P from S, dS from P and dP, held
+//               in registers and written to the dS columns after the next block's P,
+//               and at the end half of dQ's columns to global memory.  Per item they
+//               also copy their half of each Q row into TMEM.
 // TMEM (512 columns for D = 128): S [0,128), dP [128,256), dQ [256,256+D),
 // Q [256+D, 256+3D/2), dS [256+3D/2, 256+3D/2+64).
 #include "qat_internal.h"
