@@ -201,9 +201,10 @@ __global__ void __launch_bounds__(384, 1)
       auto w = [&](uint32_t b_, uint32_t par) { return mbar_wait(b_, par, abort_flag, p.err); };
       // S of block c (K tile k): after the compute warps have read S of block c - 1
       auto issue_s = [&](uint32_t k, uint32_t c, bool last) -> bool {
-        if (c > 0 && !w(bar(Q_S_EMPTY), (c - 1) & 1)) return false;
+        // the K tile first (it has almost always landed), then the compute warps' barrier
         const uint32_t st = k % kKStages;
         if (!w(bar(Q_K_FULL + st), (k / kKStages) & 1)) return false;
+        if (c > 0 && !w(bar(Q_S_EMPTY), (c - 1) & 1)) return false;
         tc_fence_after();
         const uint32_t sk = base + C::kOffK + st * C::kTileBytes;
 #pragma unroll
@@ -269,9 +270,9 @@ __global__ void __launch_bounds__(384, 1)
         ok = w(bar(Q_DO_FULL), it & 1);
         for (int j = 0; j < J && ok; ++j, ++vc, ++bc) {
           // dP overwrites dP of block bc - 1: wait until the compute warps have read it
-          if (bc > 0 && !(ok = w(bar(Q_DP_EMPTY), (bc - 1) & 1))) break;
           const uint32_t st = vc % kVStages;
           if (!(ok = w(bar(Q_V_FULL + st), (vc / kVStages) & 1))) break;
+          if (bc > 0 && !(ok = w(bar(Q_DP_EMPTY), (bc - 1) & 1))) break;
           tc_fence_after();
           const uint32_t sv = base + C::kOffV + st * C::kTileBytes;
 #pragma unroll

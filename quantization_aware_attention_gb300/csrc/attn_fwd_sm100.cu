@@ -74,7 +74,8 @@ struct FwdTc {
 enum : uint32_t {
   BAR_Q_FULL = 0, BAR_Q_EMPTY = 1, BAR_K_FULL = 2, BAR_K_EMPTY = 5, BAR_V_FULL = 8,
   BAR_V_EMPTY = 10, BAR_S_FULL = 12, BAR_P_FULL = 14, BAR_O_DONE = 16, BAR_O_EMPTY = 17,
-  BAR_DRAIN = 18, BAR_X = 19, BAR_S_FREE = 20, BAR_DRAIN_B = 22, BAR_COUNT = 23
+  BAR_DRAIN = 18, BAR_X = 19, BAR_S_FREE = 20, BAR_DRAIN_B = 22, BAR_O_FINAL = 23,
+  BAR_COUNT = 24
 };
 
 struct TcParams {
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(BAR_O_EMPTY), 256);
     mbar_init(bar(BAR_DRAIN), 1);
     mbar_init(bar(BAR_DRAIN_B), 1);
+    mbar_init(bar(BAR_O_FINAL), 1);
     mbar_init(bar(BAR_X), 256);
     fence_barrier_init();
     prefetch_tmap(&tmQ);
@@ -271,10 +273,11 @@ __global__ void __launch_bounds__(384, 1)
         const int J = kv_tiles(p, mt);
         for (int j = 0; j < J && ok; ++j, ++vc, ++pc) {
           const uint32_t b = pc & 1;
-          ok = mbar_wait(bar(BAR_P_FULL + b), (pc >> 1) & 1, abort_flag, p.err);
-          if (ok && j == 0) ok = mbar_wait(bar(BAR_O_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
+          // V first (it has almost always landed), then P from the softmax warps
           const uint32_t st = vc % kVStages;
-          if (ok) ok = mbar_wait(bar(BAR_V_FULL + st), (vc / kVStages) & 1, abort_flag, p.err);
+          ok = mbar_wait(bar(BAR_V_FULL + st), (vc / kVStages) & 1, abort_flag, p.err);
+          if (ok) ok = mbar_wait(bar(BAR_P_FULL + b), (pc >> 1) & 1, abort_flag, p.err);
+          if (ok && j == 0) ok = mbar_wait(bar(BAR_O_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
@@ -293,6 +296,7 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit(bar(BAR_V_EMPTY + st));
           mma_commit(bar(BAR_O_DONE));
           mma_commit(bar(BAR_S_FREE + b));
+          if (j + 1 == J) mma_commit(bar(BAR_O_FINAL));  // the item's O is complete
         }
       }
       if (issued) {
@@ -428,7 +432,12 @@ __global__ void __launch_bounds__(384, 1)
       xsum[h * 128 + r] = l;
       if (!(ok = exchange())) break;
       const float l_row = xsum[r] + xsum[128 + r];
-      ok = wwait(bar(BAR_O_DONE), (pvc - 1) & 1);
+      // O_DONE cannot be used here: it completes once per block, and at the end of an
+      // item the PV products of the last two blocks may both still be running (S of
+      // the last block only waited for PV two blocks back).  A parity wait on a barrier
+      // two phases behind passes at once, so the epilogue waits on O_FINAL, committed
+      // after the item's last PV: one phase per item.
+      ok = wwait(bar(BAR_O_FINAL), it & 1);
       if (!ok) break;
       tc_fence_after();
       const float inv_l = 1.0f / l_row;

@@ -155,6 +155,29 @@ def test_deterministic(causal):
         assert torch.equal(a[n], b[n]), n
 
 
+def test_forward_deterministic_causal_many_items():
+    """The c5a shape, causal: thousands of items of 1 to 64 key blocks over 152 CTAs.
+    Every output must be bit-identical across runs.  (An epilogue that waited on a
+    per-block barrier could pass while the last two PV products were still running;
+    at this size that showed as a few dozen query tiles differing run to run.)"""
+    B, H, N, D = 4, 32, 8192, 128
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    q, k, v = (torch.randn(B, H, N, D, device="cuda", generator=gen).to(torch.bfloat16)
+               for _ in range(3))
+    outs = []
+    for _ in range(3):
+        o_q, o_hp = torch.empty_like(q), torch.empty_like(q)
+        lse = torch.empty(B, H, N, device="cuda")
+        st = capi.qat_attn_fwd(q, k, v, o_q, o_hp, lse, B, H, N, N, D, 1.0 / np.sqrt(D), 1, 1)
+        assert st == Status.OK
+        torch.cuda.synchronize()
+        outs.append((o_q, o_hp, lse))
+    assert capi.qat_attn_device_status() == Status.OK
+    for o in outs[1:]:
+        for a_, b_ in zip(outs[0], o):
+            assert torch.equal(a_, b_)
+
+
 # ------------------------------------------------------------------ full-size, sampled
 
 def _sampled_full_size(name, fwd_heads, bwd_head, n_rows=256, n_keys=64):
