@@ -178,6 +178,32 @@ def test_forward_deterministic_causal_many_items():
             assert torch.equal(a_, b_)
 
 
+def test_backward_deterministic_causal_many_items():
+    """The c5a shape, causal, through the backward: dQ, dK and dV bit-identical across
+    runs (each CTA sums its own rows in a fixed order; no atomics)."""
+    B, H, N, D = 4, 32, 8192, 128
+    gen = torch.Generator(device="cuda").manual_seed(6)
+    q, k, v, do = (torch.randn(B, H, N, D, device="cuda", generator=gen).to(torch.bfloat16)
+                   for _ in range(4))
+    sm = 1.0 / np.sqrt(D)
+    o_q, o_hp = torch.empty_like(q), torch.empty_like(q)
+    lse = torch.empty(B, H, N, device="cuda")
+    assert capi.qat_attn_fwd(q, k, v, o_q, o_hp, lse, B, H, N, N, D, sm, 1, 1) == Status.OK
+    wsb = capi.qat_attn_bwd_workspace_bytes(B, H, N, N, D)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        g = [torch.empty_like(q) for _ in range(3)]
+        st = capi.qat_attn_bwd(q, k, v, o_hp, lse, do, *g, B, H, N, N, D, sm, 1, 1, ws, wsb)
+        assert st == Status.OK
+        torch.cuda.synchronize()
+        outs.append(g)
+    assert capi.qat_attn_device_status() == Status.OK
+    for o in outs[1:]:
+        for a_, b_ in zip(outs[0], o):
+            assert torch.equal(a_, b_)
+
+
 # ------------------------------------------------------------------ full-size, sampled
 
 def _sampled_full_size(name, fwd_heads, bwd_head, n_rows=256, n_keys=64):
