@@ -32,8 +32,11 @@
 //               and dP^T - Delta and the compute warps read no per-query values at all.
 //               Each stream only overwrites TMEM its own earlier MMAs read (S^T over P^T,
 //               dP^T over dS^T); operands both read (Q, dO, K/V) are released by one
-//               commit from each.  Shared-memory bandwidth bounds the kernel: per 128 x
-//               128 block the MMAs read ~208 KB and TMA writes ~72 KB.
+//               commit from each.  Each issuer waits for the next block's Q (dO) tile
+//               before the compute warps' barrier, so the next score product follows
+//               without a wait.  What bounds the kernel is the loop this in-place reuse
+//               makes: P^T_b written -> dV_b -> S^T_{b+1} -> its completion -> the next
+//               P phase (TMEM has no room for a second S^T buffer).
 //   warps 3-10  two compute warpgroups, each owning 64 of a block's 128 query columns:
 //               P phase (P^T = exp2(qk_scale (S^T - lse / qk_scale)), bf16 over the
 //               group's S^T columns), dS phase (dS^T = P^T o (dP^T - Delta), bf16 over the
