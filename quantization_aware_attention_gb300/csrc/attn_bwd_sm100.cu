@@ -586,69 +586,63 @@ __device__ __forceinline__ void bf16_split3(float x, uint16_t (&t)[3]) {
   }
 }
 
-// One warp per padded query row: Delta, the lse copy (+inf in padding rows), and the
-// row's lse_ext / d_ext entries (-lse / qk_scale and -Delta as three bf16 terms; padding
-// rows get -1e30 and 0, so P = 0 there).  Block 0 also writes the ones tile.
+// Per padded query row: Delta, the lse copy (+inf in padding rows), and the row's
+// lse_ext / d_ext entries (-lse / qk_scale and -Delta as three bf16 terms; padding rows
+// get -1e30 and 0, so P = 0 there).  D / 8 lanes cover a row with 16-byte loads, so a
+// warp has 32 / (D / 8) rows in flight per pass.  Block 0 also writes the ones tile.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x)
       a.ones[i] = (i & 15) < 3 ? 0x3F80u : 0u;   // bf16 1.0 in elements 0-2
-  constexpr int PER = D / 32;
+  constexpr int kLanesPerRow = D / 8;          // 8 bf16 per lane
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const long long rows = static_cast<long long>(a.B) * a.H * nq_pad;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
-  for (long long rw = warp0; rw < rows; rw += nw) {
-    const long long bh = rw / nq_pad;
-    const int q = static_cast<int>(rw % nq_pad);
-    if (q >= a.Nq) {
-      if (lane == 0) {
-        a.delta[rw] = 0.f;
-        a.lse_pad[rw] = INFINITY;
-      }
-      if (lane < 16) {
-        uint16_t t[3];
-        bf16_split3(-1e30f, t);
-        a.lse_ext[rw * 16 + lane] = lane == 0 ? t[0] : lane == 1 ? t[1] : lane == 2 ? t[2] : 0u;
-        a.d_ext[rw * 16 + lane] = 0u;
-      }
-      continue;
-    }
-    const long long src = (bh * a.Nq + q) * D + lane * PER;
+  const int sub = lane % kLanesPerRow, slot = lane / kLanesPerRow;
+  for (long long first = warp0 * kRowsPerWarp; first < rows; first += nw * kRowsPerWarp) {
+    const long long rw = first + slot;
+    const bool valid = rw < rows;
+    const long long bh = valid ? rw / nq_pad : 0;
+    const int q = valid ? static_cast<int>(rw % nq_pad) : 0;
+    const bool in = valid && q < a.Nq;
     float acc = 0.f;
-    if constexpr (PER == 4) {
-      const uint2 ov = *reinterpret_cast<const uint2*>(a.o_hp + src);
-      const uint2 dv = *reinterpret_cast<const uint2*>(a.dO + src);
+    if (in) {
+      const long long src = (bh * a.Nq + q) * D + 8 * sub;
+      const uint4 ov = *reinterpret_cast<const uint4*>(a.o_hp + src);
+      const uint4 dv = *reinterpret_cast<const uint4*>(a.dO + src);
       const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
       const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const float2 of = __bfloat1622float2(o2[i]);
         const float2 df = __bfloat1622float2(d2[i]);
         acc = fmaf(of.x, df.x, acc);
         acc = fmaf(of.y, df.y, acc);
       }
-    } else {
-      const uint32_t ov = *reinterpret_cast<const uint32_t*>(a.o_hp + src);
-      const uint32_t dv = *reinterpret_cast<const uint32_t*>(a.dO + src);
-      const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
-      const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv));
-      acc = fmaf(of.x, df.x, of.y * df.y);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    const float lse = a.lse[bh * a.Nq + q];
-    if (lane == 0) {
-      a.delta[rw] = acc;
-      a.lse_pad[rw] = lse;
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)   // within the row's lanes
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (!valid) continue;
+    const float lse = in ? a.lse[bh * a.Nq + q] : 0.f;
+    if (sub == 0) {
+      a.delta[rw] = in ? acc : 0.f;
+      a.lse_pad[rw] = in ? lse : INFINITY;
     }
-    if (lane < 16) {                                 // every lane holds the full sum
-      uint16_t tl[3], td[3];
-      bf16_split3(-lse / a.qk_scale, tl);
-      bf16_split3(-acc, td);
-      a.lse_ext[rw * 16 + lane] = lane == 0 ? tl[0] : lane == 1 ? tl[1] : lane == 2 ? tl[2] : 0u;
-      a.d_ext[rw * 16 + lane] = lane == 0 ? td[0] : lane == 1 ? td[1] : lane == 2 ? td[2] : 0u;
+    if (sub < 2) {                    // elements 8 sub .. 8 sub + 7 of both ext rows
+      uint4 el = make_uint4(0u, 0u, 0u, 0u), ed = make_uint4(0u, 0u, 0u, 0u);
+      if (sub == 0) {
+        uint16_t tl[3], td[3];
+        bf16_split3(in ? -lse / a.qk_scale : -1e30f, tl);
+        bf16_split3(in ? -acc : 0.f, td);
+        el = make_uint4(tl[0] | (static_cast<uint32_t>(tl[1]) << 16), tl[2], 0u, 0u);
+        ed = make_uint4(td[0] | (static_cast<uint32_t>(td[1]) << 16), td[2], 0u, 0u);
+      }
+      *reinterpret_cast<uint4*>(a.lse_ext + rw * 16 + 8 * sub) = el;
+      *reinterpret_cast<uint4*>(a.d_ext + rw * 16 + 8 * sub) = ed;
     }
   }
 }
@@ -666,7 +660,8 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   p.nq_pad = p.mtiles * kBlk;
 
   const long long prow = static_cast<long long>(BH) * p.nq_pad;
-  long long pblocks = (prow + 7) / 8;
+  constexpr long long kPrepRowsPerBlock = 8 * (256 / D);  // 8 warps of 32 / (D / 8) rows
+  long long pblocks = (prow + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock;
   if (pblocks > static_cast<long long>(num_sms) * 64) pblocks = static_cast<long long>(num_sms) * 64;
   bwd_prep_kernel<D><<<static_cast<unsigned>(pblocks), 256, 0, s>>>(a, p.nq_pad);
   cudaError_t e = cudaGetLastError();
