@@ -458,7 +458,8 @@ def run_ours(args, w):
         barrier()
         ch_ms = ev[0].elapsed_time(ev[1])
         merge_ms = ev[1].elapsed_time(ev[2]) / (nch - 1)
-        merge_bytes = 4 * B * H * Nq * (4 * D + 3)  # read acc + part, write acc (O_q, O_hp, lse)
+        # read acc and part, write acc: 3 x (O_q, O_hp, lse) = 3 (2D + 1) fp32 per row
+        merge_bytes = 4 * B * H * Nq * 3 * (2 * D + 1)
         chunked = {"chunks": nch, "ms": ch_ms, "tflops": 6.0 * pairs_of(w) * D / (ch_ms * 1e-3) / 1e12,
                    "one_pass_fwd_ms": None, "merge_ms": merge_ms,
                    "merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9,
