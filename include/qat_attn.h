@@ -250,6 +250,18 @@ QAT_API qat_status_t qat_attn_device_status(void* stream);
 QAT_API qat_status_t qat_debug_quant_tiles(const float* p, int rows, int cols, float* deq,
                                    float* scales, unsigned char* codes, void* stream);
 
+/*
+ * qat_debug_wait_timeout -- test entry for the failure path of the kernels' bounded
+ * waits: one thread waits, with the same bounded mbarrier wait the attention kernels use,
+ * on a barrier nothing arrives on.  After limit_ms milliseconds the wait gives up, sets
+ * the device error word and the kernel returns normally (no fault, trap or hang), so the
+ * next qat_attn_device_status(stream) returns QAT_ERR_TIMEOUT and clears the word.  The
+ * page has no counterpart; this entry exists for the tests.
+ *   limit_ms  1 .. 4000
+ * Errors: QAT_ERR_INVALID_ARG (limit out of range), QAT_ERR_CUDA (launch error).
+ */
+QAT_API qat_status_t qat_debug_wait_timeout(int limit_ms, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

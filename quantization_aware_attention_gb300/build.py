@@ -21,7 +21,7 @@ OBJDIR = os.path.join(HERE, "_build_tmp")
 LIB_PATH = os.path.join(HERE, "libqat_attn.so")
 
 SOURCES = ["qat_api.cu", "attn_fwd_sm100.cu", "attn_bwd_sm100.cu", "attn_bwd_dq_sm100.cu",
-           "quant_debug.cu", "qat_noalloc.cu", "qkv_quant.cu", "attn_merge.cu"]
+           "quant_debug.cu", "qat_noalloc.cu", "qkv_quant.cu", "attn_merge.cu", "debug_wait.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",

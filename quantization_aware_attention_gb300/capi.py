@@ -25,6 +25,7 @@ EXPORTED = (
     "qat_status_string",
     "qat_attn_device_status",
     "qat_debug_quant_tiles",
+    "qat_debug_wait_timeout",
     "qat_channel_mean",
     "qat_fake_quant_tokens",
     "qat_attn_fwd_chunk",
@@ -79,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.qat_attn_device_status.restype = _i
         L.qat_debug_quant_tiles.argtypes = [_vp, _i, _i, _vp, _vp, _vp, _vp]
         L.qat_debug_quant_tiles.restype = _i
+        L.qat_debug_wait_timeout.argtypes = [_i, _vp]
+        L.qat_debug_wait_timeout.restype = _i
         L.qat_channel_mean.argtypes = [_vp, _vp] + [_i] * 4 + [_vp]
         L.qat_channel_mean.restype = _i
         L.qat_fake_quant_tokens.argtypes = [_vp] * 4 + [_i] * 4 + [_vp]
@@ -141,6 +144,10 @@ def qat_attn_bwd_noalloc(q, k, v, o_hp, lse, dO, dq, dk, dv, B, H, Nq, Nkv, D, s
 
 def qat_attn_device_status(stream=None) -> Status:
     return Status(lib().qat_attn_device_status(_stream(stream)))
+
+
+def qat_debug_wait_timeout(limit_ms, stream=None) -> Status:
+    return Status(lib().qat_debug_wait_timeout(limit_ms, _stream(stream)))
 
 
 def qat_debug_quant_tiles(p, rows, cols, deq, scales, codes, stream=None) -> Status:

@@ -108,6 +108,12 @@ def test_debug_quant_validation():
     assert capi.qat_debug_quant_tiles(None, 0, 64, None, None, None, stream=0) == Status.OK
 
 
+def test_wait_timeout_validation():
+    # rejected before anything touches the device
+    assert capi.qat_debug_wait_timeout(0, stream=0) == Status.INVALID_ARG
+    assert capi.qat_debug_wait_timeout(4001, stream=0) == Status.INVALID_ARG
+
+
 def test_chunk_and_merge_validation():
     base = dict(q=A, k=A, v=A, o_q=A, o_hp=A, lse=A, B=1, H=1, Nq=8, Nkv_total=256, D=128,
                 sm_scale=0.1, quant_mode=1, stream=0)

@@ -155,6 +155,17 @@ def test_deterministic(causal):
         assert torch.equal(a[n], b[n]), n
 
 
+def test_expired_wait_is_reported_then_cleared():
+    """The failure path of the kernels' bounded waits: the test entry waits on a barrier
+    nothing arrives on, gives up after 50 ms and sets the device error word; the next
+    status read reports QAT_ERR_TIMEOUT and clears it, and the context stays usable."""
+    assert capi.qat_debug_wait_timeout(50) == Status.OK
+    assert capi.qat_attn_device_status() == Status.TIMEOUT
+    assert capi.qat_attn_device_status() == Status.OK
+    inp = custom_inputs(123, 1, 2, 200, 200, 128)
+    check_full(inp, True, 1.0 / np.sqrt(128))
+
+
 def test_forward_deterministic_causal_many_items():
     """The c5a shape, causal: thousands of items of 1 to 64 key blocks over 152 CTAs.
     Every output must be bit-identical across runs.  (An epilogue that waited on a
