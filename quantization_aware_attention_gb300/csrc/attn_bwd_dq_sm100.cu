@@ -80,13 +80,15 @@ struct DqParams {
   int ntiles;   // key blocks per head
   int items;    // B * H * mtiles
   int nq_pad;   // mtiles * 128
+  int hgroup;   // heads per group of the causal order (causal_head_group)
 };
 
 __device__ __forceinline__ void dq_item(int idx, const DqParams& p, int& bh, int& mt, int& J) {
   const int BH = p.a.B * p.a.H;
-  if (p.a.causal) {  // longest first: late query blocks see the most keys
-    mt = p.mtiles - 1 - idx / BH;
-    bh = idx % BH;
+  if (p.a.causal) {  // longest first (late query blocks see the most keys), heads in groups
+    int cls;
+    causal_item(idx, BH, p.mtiles, p.hgroup, bh, cls);
+    mt = p.mtiles - 1 - cls;
     J = min(p.ntiles, mt + 1);
   } else {           // head-major: the CTAs running together share one head's K/V in L2
     bh = idx / p.mtiles;
@@ -457,6 +459,8 @@ cudaError_t launch_bwd_dq_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   p.ntiles = (a.Nkv + kBlk - 1) / kBlk;
   p.items = BH * p.mtiles;
   p.nq_pad = p.mtiles * kBlk;
+  // a causal item streams its head's K and V blocks
+  p.hgroup = causal_head_group(4ll * a.Nkv * D, BH);
   CUtensorMap mk, mv, mdo;
   if (!make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) || !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) ||
       !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH))

@@ -94,14 +94,14 @@ struct BwdTcParams {
   int ktiles;   // key blocks per head
   int items;    // B * H * ktiles
   int nq_pad;   // mtiles * 128
+  int hgroup;   // heads per group of the causal order (causal_head_group)
 };
 
 __device__ __forceinline__ void bwd_item(int idx, const BwdTcParams& p, int& bh, int& kb,
                                          int& first, int& count) {
   const int BH = p.a.B * p.a.H;
-  if (p.a.causal) {  // longest first: small key blocks see the most queries
-    kb = idx / BH;
-    bh = idx % BH;
+  if (p.a.causal) {  // longest first (small key blocks see the most queries), heads in groups
+    causal_item(idx, BH, p.ktiles, p.hgroup, bh, kb);
     first = kb;
     count = p.mtiles - kb;
   } else {           // head-major: the CTAs running together share one head's Q/dO in L2
@@ -658,6 +658,8 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   p.ktiles = (a.Nkv + kBlk - 1) / kBlk;
   p.items = BH * p.ktiles;
   p.nq_pad = p.mtiles * kBlk;
+  // a causal item streams its head's Q and dO blocks
+  p.hgroup = causal_head_group(4ll * a.Nq * D, BH);
 
   const long long prow = static_cast<long long>(BH) * p.nq_pad;
   constexpr long long kPrepRowsPerBlock = 8 * (256 / D);  // 8 warps of 32 / (D / 8) rows

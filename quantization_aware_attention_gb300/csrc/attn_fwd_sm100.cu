@@ -83,13 +83,15 @@ struct TcParams {
   unsigned int* err;
   int mtiles;   // ceil(Nq / 128)
   int items;    // B * H * mtiles
+  int hgroup;   // heads per group of the causal order (causal_head_group)
 };
 
 __device__ __forceinline__ void item_coords(int idx, const TcParams& p, int& bh, int& mt) {
   const int BH = p.a.B * p.a.H;
-  if (p.a.causal) {  // longest rows first
-    mt = p.mtiles - 1 - idx / BH;
-    bh = idx % BH;
+  if (p.a.causal) {  // longest rows first, heads in L2-sized groups
+    int cls;
+    causal_item(idx, BH, p.mtiles, p.hgroup, bh, cls);
+    mt = p.mtiles - 1 - cls;
   } else {           // head-major: CTAs running together share one head's K/V in L2
     bh = idx / p.mtiles;
     mt = idx % p.mtiles;
@@ -501,6 +503,8 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a, unsigned int* err, int num_sms, cu
   p.err = err;
   p.mtiles = (a.Nq + kBM - 1) / kBM;
   p.items = BH * p.mtiles;
+  // a causal item streams its head's K and V blocks
+  p.hgroup = causal_head_group(4ll * a.Nkv * D, BH);
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::kSmemBytes));

@@ -98,6 +98,35 @@ cudaError_t launch_merge(float* o_q_acc, float* o_hp_acc, float* lse_acc, const 
 cudaError_t launch_debug_quant(const float* p, int rows, int cols, float* deq,
                                float* scales, uint8_t* codes, cudaStream_t s);
 
+// Causal work order.  A causal item (one head x one 128-row block) has between 1 and M
+// blocks of work, so the persistent kernels take the longest items first.  Heads are
+// taken in groups: inside a group the length classes descend and the group's heads
+// alternate within a class, so the CTAs running together touch only a group or two of
+// heads and the K/V (or Q/dO) blocks they all stream stay in L2.  With every head in
+// one group the order is pure longest-first, which leaves a wave on as many heads as
+// there are CTAs and has each CTA fetch its head's blocks from DRAM.
+inline int causal_head_group(long long bytes_per_head, int BH) {
+  constexpr long long kGroupBytes = 32ll << 20;  // a wave spans about two groups of L2
+  long long g = kGroupBytes / (bytes_per_head > 0 ? bytes_per_head : 1);
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  return static_cast<int>(g);
+}
+
+#ifdef __CUDACC__
+// Item idx of that order -> head bh and length class cls (0 = the longest, M blocks).
+__device__ __forceinline__ void causal_item(int idx, int BH, int M, int hgroup, int& bh,
+                                            int& cls) {
+  const int per = hgroup * M;
+  const int gi = idx / per;
+  const int h0 = gi * hgroup;
+  const int hs = min(hgroup, BH - h0);
+  const int j = idx - gi * per;
+  cls = j / hs;
+  bh = h0 + (j - cls * hs);
+}
+#endif
+
 // Device-side error word (bounded waits set it); defined in qat_api.cu.
 cudaError_t read_and_clear_device_error(unsigned int* out, cudaStream_t s);
 // Device address of that word and the SM count, for the current device (cached).
