@@ -63,7 +63,8 @@ struct FwdTc {
   static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr uint32_t kOffMisc = kOffBar + 256;
   static constexpr uint32_t kOffX = kOffMisc + 64;     // row-max / row-sum exchange, 3 KB
-  static constexpr uint32_t kUsed = kOffX + 3072;
+  static constexpr uint32_t kOffStage = kOffX + 3072;  // epilogue staging, 2 KB per softmax warp
+  static constexpr uint32_t kUsed = kOffStage + 8 * 2048;
   // at least 116 KB so that no two CTAs share an SM (each holds all 512 TMEM columns)
   static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
   static constexpr uint32_t kTmemOq = 256;
@@ -317,6 +318,24 @@ __global__ void __launch_bounds__(384, 1)
     const float qk = p.a.qk_scale;
     float* xmax = reinterpret_cast<float*>(gbase + C::kOffX);        // [2 parity][2 h][128]
     float* xsum = reinterpret_cast<float*>(gbase + C::kOffX + 2048); // [2 h][128]
+    // Epilogue stores: 64 bytes of each of the warp's 32 rows (this thread's row is its
+    // lane) go through the warp's 2 KB of shared memory, with the 16-byte chunks XOR-
+    // swizzled by row so that the row-wise writes and the column-wise reads are both free
+    // of bank conflicts.  Read back, one store instruction writes 8 rows x 64 bytes (16
+    // full sectors) instead of 32 rows x 16 bytes (32 half sectors).
+    uint4* stg = reinterpret_cast<uint4*>(gbase + C::kOffStage) + (warp - 3) * 128;
+    auto store_rows64 = [&](const uint4 (&v)[4], char* row0, size_t row_bytes, int rows_valid) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) stg[lane * 4 + (i ^ ((lane >> 1) & 3))] = v[i];
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rr = 8 * k + (lane >> 2), cc = lane & 3;
+        const uint4 x = stg[rr * 4 + (cc ^ ((rr >> 1) & 3))];
+        if (rr < rows_valid) *reinterpret_cast<uint4*>(row0 + rr * row_bytes + 16 * cc) = x;
+      }
+      __syncwarp();  // the next call overwrites the staging
+    };
     // tcgen05.ld/st are warp-collective: every wait result is made warp-uniform
     auto wwait = [&](uint32_t b_, uint32_t par) {
       const bool w = mbar_wait(b_, par, abort_flag, p.err);
@@ -444,7 +463,10 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const float inv_l = 1.0f / l_row;
       const bool in = row < p.a.Nq;
-      const size_t orow = (static_cast<size_t>(bh) * p.a.Nq + (in ? row : 0)) * D;
+      // the warp's first row, and how many of its 32 rows exist
+      const int wrow = mt * kBM + 32 * quarter;
+      const int wvalid = min(32, p.a.Nq - wrow);
+      const size_t orow0 = static_cast<size_t>(bh) * p.a.Nq + wrow;
       const uint32_t tO = tbase + lrow + (h ? C::kTmemOhp : C::kTmemOq);
       uint16_t* out = h ? p.a.o_hp : p.a.o_q;
       float* out32 = h ? p.a.o_hp_f32 : p.a.o_q_f32;  // partial results stay fp32
@@ -454,12 +476,19 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
         if (out32 != nullptr) {
-          if (in) {
-            float4* dst = reinterpret_cast<float4*>(out32 + orow + 32 * c);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          for (int half = 0; half < 2; ++half) {
+            uint4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t* x = o + 16 * half + 4 * i;
+              v[i] = make_uint4(__float_as_uint(__uint_as_float(x[0]) * inv_l),
+                                __float_as_uint(__uint_as_float(x[1]) * inv_l),
+                                __float_as_uint(__uint_as_float(x[2]) * inv_l),
+                                __float_as_uint(__uint_as_float(x[3]) * inv_l));
+            }
+            store_rows64(v, reinterpret_cast<char*>(out32 + orow0 * D + 32 * c + 16 * half),
+                         D * sizeof(float), wvalid);
           }
           continue;
         }
@@ -467,12 +496,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (in) {
-          uint4* dst = reinterpret_cast<uint4*>(out + orow + 32 * c);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-        }
+        const uint4 v[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
+                            make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
+        store_rows64(v, reinterpret_cast<char*>(out + orow0 * D + 32 * c), D * sizeof(uint16_t), wvalid);
       }
       // (xsum is rewritten only after the next item's first exchange, which both
       // groups reach after this read)
