@@ -92,30 +92,47 @@ struct BwdTcParams {
   unsigned int* err;
   int mtiles;   // query blocks per head
   int ktiles;   // key blocks per head
-  int items;    // B * H * ktiles
+  int items;    // B * H * ktiles * nsplit
   int nq_pad;   // mtiles * 128
   int hgroup;   // heads per group of the causal order (causal_head_group)
+  int nsplit;   // query parts per (head, key block) when non-causal (bwd_key_split)
 };
 
-__device__ __forceinline__ void bwd_item(int idx, const BwdTcParams& p, int& bh, int& kb,
-                                         int& first, int& count) {
+// One dK/dV item: key block kb of head bh over `count` query blocks starting at q0.
+// Non-causal items walk their range from a rotated start (rot), so that the CTAs of one
+// head do not all read the same query block at once; part is the item's query part
+// (0 unless the items are split, bwd_key_split).
+struct BwdItem {
+  int bh, kb, q0, count, rot, part;
+};
+
+__device__ __forceinline__ BwdItem bwd_item(int idx, const BwdTcParams& p) {
   const int BH = p.a.B * p.a.H;
+  BwdItem t;
   if (p.a.causal) {  // longest first (small key blocks see the most queries), heads in groups
-    causal_item(idx, BH, p.ktiles, p.hgroup, bh, kb);
-    first = kb;
-    count = p.mtiles - kb;
+    causal_item(idx, BH, p.ktiles, p.hgroup, t.bh, t.kb);
+    t.q0 = t.kb;
+    t.count = p.mtiles - t.kb;
+    t.rot = 0;
+    t.part = 0;
   } else {           // head-major: the CTAs running together share one head's Q/dO in L2
-    bh = idx / p.ktiles;
-    kb = idx % p.ktiles;
-    first = kb % p.mtiles;
-    count = p.mtiles;
+    const int per_head = p.ktiles * p.nsplit;
+    t.bh = idx / per_head;
+    const int rem = idx - t.bh * per_head;
+    t.kb = rem / p.nsplit;
+    t.part = rem - t.kb * p.nsplit;
+    t.q0 = (t.part * p.mtiles) / p.nsplit;
+    t.count = ((t.part + 1) * p.mtiles) / p.nsplit - t.q0;
+    t.rot = t.kb % t.count;
   }
+  return t;
 }
 
-__device__ __forceinline__ int block_at(int first, int ii, const BwdTcParams& p) {
-  int b = first + ii;
-  if (!p.a.causal && b >= p.mtiles) b -= p.mtiles;
-  return b;
+// query block of the item's ii-th step
+__device__ __forceinline__ int block_at(const BwdItem& t, int ii) {
+  int b = t.rot + ii;
+  if (b >= t.count) b -= t.count;
+  return t.q0 + b;
 }
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -202,8 +219,8 @@ __global__ void __launch_bounds__(384, 1)
         return true;
       };
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-        int bh, kb, first, count;
-        bwd_item(idx, p, bh, kb, first, count);
+        const BwdItem t = bwd_item(idx, p);
+        const int bh = t.bh, kb = t.kb, count = t.count;
         ok = mbar_wait(bar(B_KV_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::kTileBytes);
@@ -213,9 +230,9 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(base + C::kOffV + c * C::kChunkBytes, &tmV, bar(B_KV_FULL), 64 * c,
                       kb * kBlk, bh);
         }
-        ok = load_q(bh, block_at(first, 0, p));
+        ok = load_q(bh, block_at(t, 0));
         for (int ii = 0; ii < count && ok; ++ii) {
-          const int blk = block_at(first, ii, p);
+          const int blk = block_at(t, ii);
           const uint32_t dst = dc & 1, duse = dc >> 1;
           ok = mbar_wait(bar(B_DO_EMPTY0 + dst), (duse & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
@@ -226,7 +243,7 @@ __global__ void __launch_bounds__(384, 1)
                         64 * c, blk * kBlk, bh);
           tma_load_3d(base + C::kOffDX + dst * C::kExtBytes, &tmDX, fb, 0, blk * kBlk, bh);
           ++dc;
-          if (ii + 1 < count) ok = load_q(bh, block_at(first, ii + 1, p));
+          if (ii + 1 < count) ok = load_q(bh, block_at(t, ii + 1));
         }
       }
       // drain: every issued load lands before the CTA exits
@@ -266,8 +283,7 @@ __global__ void __launch_bounds__(384, 1)
       };
       ok = w(bar(B_ONES_FULL), 0);
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-        int bh, kb, first, count;
-        bwd_item(idx, p, bh, kb, first, count);
+        const int count = bwd_item(idx, p).count;
         ok = w(bar(B_KV_FULL), it & 1) && wait_q(qc);
         if (ok) issue_s(qc);
         for (int ii = 0; ii < count && ok; ++ii, ++qc) {
@@ -333,8 +349,7 @@ __global__ void __launch_bounds__(384, 1)
       };
       ok = w(bar(B_ONES_FULL), 0);
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-        int bh, kb, first, count;
-        bwd_item(idx, p, bh, kb, first, count);
+        const int count = bwd_item(idx, p).count;
         ok = w(bar(B_KV_FULL), it & 1) && wait_do(qc);
         if (ok) issue_dp(qc);
         for (int ii = 0; ii < count && ok; ++ii, ++qc) {
@@ -523,8 +538,8 @@ __global__ void __launch_bounds__(384, 1)
     int it = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-      int bh, kb, first, count;
-      bwd_item(idx, p, bh, kb, first, count);
+      const BwdItem t = bwd_item(idx, p);
+      const int bh = t.bh, kb = t.kb, count = t.count;
       const int key = kb * kBlk + r;
       const bool key_ok = key < p.a.Nkv;
       // order per block b: dS_b, then P_{b+1}, which is ready before dV_{b+1} is issued
@@ -532,10 +547,10 @@ __global__ void __launch_bounds__(384, 1)
         return p.a.page_bwd ? p_phase_page(c_, blk_, kb, key_ok, key)
                             : p_phase(c_, blk_, kb, key_ok, key);
       };
-      ok = pp(qc, block_at(first, 0, p));
+      ok = pp(qc, block_at(t, 0));
       for (int ii = 0; ii < count && ok; ++ii, ++qc) {
         ok = ds_phase(qc);
-        if (ok && ii + 1 < count) ok = pp(qc + 1, block_at(first, ii + 1, p));
+        if (ok && ii + 1 < count) ok = pp(qc + 1, block_at(t, ii + 1));
       }
       if (!ok) break;
       // ---- epilogue: h = 0 stores dV, h = 1 stores dK for this item's key rows
@@ -546,11 +561,24 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t tcol = h ? C::kTmemDK : C::kTmemDV;
       uint16_t* out = h ? p.a.dk : p.a.dv;
       const float scale = h ? p.a.sm_scale : 1.0f;
+      // a query part stores its fp32 partial sums (dK unscaled); bwd_part_sum_kernel
+      // adds the parts in order and converts
+      float* part = p.nsplit > 1
+                        ? p.a.part + (static_cast<size_t>(t.part) * 2 + h) * p.a.B * p.a.H * p.a.Nkv * D + grow
+                        : nullptr;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         tmem_ld32(tbase + lrow + tcol + 32 * c, ov);
         tmem_wait_ld();
+        if (part != nullptr) {
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(part + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) dst[v] = make_uint4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
+          }
+          continue;
+        }
         uint32_t wv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -647,6 +675,29 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
   }
 }
 
+// Adds the query parts' partial sums of dV and dK in part order and stores them as bf16
+// (dK times sm_scale): n4 float4s per tensor, parts laid out [part][dV, dK][n4].
+__global__ void __launch_bounds__(256) bwd_part_sum_kernel(const float4* __restrict__ part,
+                                                           int nsplit, long long n4,
+                                                           float sm_scale, uint2* dv, uint2* dk) {
+  const long long stride = static_cast<long long>(gridDim.x) * 256;
+  for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < 2 * n4;
+       i += stride) {
+    const int t = i >= n4 ? 1 : 0;
+    const long long j = i - t * n4;
+    float4 acc = part[t * n4 + j];
+    for (int s = 1; s < nsplit; ++s) {
+      const float4 x = part[(2ll * s + t) * n4 + j];
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    const float sc = t ? sm_scale : 1.0f;
+    (t ? dk : dv)[j] = make_uint2(pack_bf16x2(acc.x * sc, acc.y * sc), pack_bf16x2(acc.z * sc, acc.w * sc));
+  }
+}
+
 template <int D>
 cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s) {
   using C = BwdTc<D>;
@@ -656,7 +707,8 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   p.err = err;
   p.mtiles = (a.Nq + kBlk - 1) / kBlk;
   p.ktiles = (a.Nkv + kBlk - 1) / kBlk;
-  p.items = BH * p.ktiles;
+  p.nsplit = a.causal || a.part == nullptr ? 1 : a.nsplit;
+  p.items = BH * p.ktiles * p.nsplit;
   p.nq_pad = p.mtiles * kBlk;
   // a causal item streams its head's Q and dO blocks
   p.hgroup = causal_head_group(4ll * a.Nq * D, BH);
@@ -682,6 +734,16 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, mqx, mdx, mones, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.nsplit > 1) {
+    const long long n4 = static_cast<long long>(BH) * a.Nkv * D / 4;
+    long long blocks = (2 * n4 + 255) / 256;
+    if (blocks > static_cast<long long>(num_sms) * 16) blocks = static_cast<long long>(num_sms) * 16;
+    bwd_part_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(a.part), p.nsplit, n4, a.sm_scale,
+        reinterpret_cast<uint2*>(a.dv), reinterpret_cast<uint2*>(a.dk));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   return launch_bwd_dq(a, err, num_sms, s);
 }
 

@@ -61,12 +61,14 @@ extern "C" qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const
                                              int B, int H, int Nq, int Nkv, int D,
                                              float sm_scale, int causal, int quant_mode,
                                              void* stream) {
-  const size_t need = qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D);
   // Invalid sizes, or no query rows: qat_attn_bwd validates and needs no scratch.
-  if (need == 0 || B == 0 || H == 0 || Nq == 0)
+  if (qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D) == 0 || B == 0 || H == 0 || Nq == 0)
     return qat_attn_bwd(q, k, v, o_hp, lse, dO, dq, dk, dv, B, H, Nq, Nkv, D, sm_scale, causal,
                         quant_mode, nullptr, 0, stream);
-  if (need > kNoAllocScratchBytes) return QAT_ERR_WORKSPACE;
+  // the scratch must hold the workspace without the dK/dV query-part sums; qat_attn_bwd
+  // uses the split only when those fit as well
+  if (qat::bwd_workspace_layout(B, H, Nq, Nkv, D, 1).total > kNoAllocScratchBytes)
+    return QAT_ERR_WORKSPACE;
   const void* ptrs[] = {q, k, v, o_hp, lse, dO, dq, dk, dv};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return QAT_ERR_INVALID_ARG;

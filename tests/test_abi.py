@@ -95,6 +95,24 @@ def test_backward_validation(kw, want):
     assert bwd(**kw) == want
 
 
+def _base_workspace(B, H, Nq):
+    """The workspace without dK/dV query parts: lse and Delta (fp32), the two 16-element
+    bf16 extension rows per padded query row, and the 128 x 16 bf16 ones tile."""
+    up = lambda x: (x + 255) // 256 * 256
+    rows = B * H * ((Nq + 127) // 128 * 128)
+    return 2 * up(rows * 4) + 2 * up(rows * 32) + up(128 * 32)
+
+
+def test_workspace_holds_query_part_sums_only_for_few_key_items():
+    # c4: 10240 (head, key block) items, no split
+    assert capi.qat_attn_bwd_workspace_bytes(1, 40, 32768, 32768, 128) == _base_workspace(1, 40, 32768)
+    # c5b: 160 items of 128 query blocks on a 152-SM grid -> 4 query parts of fp32 dV, dK
+    extra = capi.qat_attn_bwd_workspace_bytes(1, 40, 16384, 512, 128) - _base_workspace(1, 40, 16384)
+    assert extra == 4 * 2 * 40 * 512 * 128 * 4
+    # fewer than 8 query blocks: never split
+    assert capi.qat_attn_bwd_workspace_bytes(1, 1, 896, 100, 64) == _base_workspace(1, 1, 896)
+
+
 def test_workspace_bytes():
     assert capi.qat_attn_bwd_workspace_bytes(1, 40, 32768, 32768, 128) >= 40 * 32768 * 4
     assert capi.qat_attn_bwd_workspace_bytes(2, 4, 8, 8, 64) % 256 == 0

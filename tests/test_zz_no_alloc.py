@@ -38,7 +38,8 @@ def _rel(a, b):
 
 
 def test_noalloc_matches_workspace_entry_on_two_calls():
-    problems = [((1, 3, 200, 200, 128), True, 11), ((2, 2, 77, 150, 64), False, 12)]
+    problems = [((1, 3, 200, 200, 128), True, 11), ((2, 2, 77, 150, 64), False, 12),
+                ((1, 1, 2000, 130, 64), False, 13)]  # the last splits its dK/dV items
     for (B, H, Nq, Nkv, D), causal, seed in problems:
         inp = custom_inputs(seed, B, H, Nq, Nkv, D)
         q, k, v, do = (_dev(inp[n]) for n in ("q", "k", "v", "do"))
