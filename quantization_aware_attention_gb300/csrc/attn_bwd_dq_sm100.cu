@@ -97,6 +97,10 @@ __device__ __forceinline__ void dq_item(int idx, const DqParams& p, int& bh, int
   }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -345,6 +349,19 @@ __global__ void __launch_bounds__(384, 1)
       const size_t prow = static_cast<size_t>(bh) * p.nq_pad + row;
       const float lse_r = p.a.lse_pad[prow];
       const float delta_r = p.a.delta[prow];
+      {  // the next item's Q half-row, lse and Delta, read at its start, into L2 now
+        const int nidx = idx + static_cast<int>(gridDim.x);
+        if (nidx < p.items) {
+          int nbh, nmt, nJ;
+          dq_item(nidx, p, nbh, nmt, nJ);
+          const int nrow = nmt * kBlk + r;
+          const size_t nprow = static_cast<size_t>(nbh) * p.nq_pad + nrow;
+          if (nrow < p.a.Nq)
+            prefetch_l2(p.a.q + (static_cast<size_t>(nbh) * p.a.Nq + nrow) * D + (D / 2) * h);
+          prefetch_l2(p.a.lse_pad + nprow);
+          prefetch_l2(p.a.delta + nprow);
+        }
+      }
       // dS of block c (keys [64h, 64h + 64)) -> TMEM dS columns [32h, 32h + 32), once dQ
       // of block c - 1 has read the buffer.  dS_c is held in registers and written after
       // P of block c + 1 has been computed, so dQ_{c-1} has a block's time to complete.
