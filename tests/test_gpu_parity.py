@@ -168,6 +168,32 @@ def test_deterministic_with_query_parts():
         assert torch.equal(a[n], b[n]), n
 
 
+def test_query_part_split_without_room_for_its_sums_runs_unsplit():
+    """A workspace that holds everything but the dK/dV parts' partial sums (as the no-alloc
+    scratch may) runs the backward without the split: the same gradients up to the fp32
+    summation order.  One byte less than that is refused."""
+    B, H, Nq, Nkv, D, sc = 1, 1, 2000, 130, 64, 0.125
+    inp = custom_inputs(94, B, H, Nq, Nkv, D)
+    q, k, v, do = (dev_bf16(inp[n]) for n in ("q", "k", "v", "do"))
+    _, o_hp, lse = qat_attention_forward(q, k, v, False, sc)
+    full = capi.qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D)
+    base = full - 4 * 2 * B * H * Nkv * D * 4  # 4 query parts of fp32 dV and dK
+    outs = {}
+    for name, nbytes in (("split", full), ("unsplit", base)):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        g = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+        st = capi.qat_attn_bwd(q, k, v, o_hp, lse, do, *g, B, H, Nq, Nkv, D, sc, 0, 1, ws, nbytes)
+        torch.cuda.synchronize()
+        assert st == Status.OK and capi.qat_attn_device_status() == Status.OK
+        outs[name] = g
+    for a, b in zip(outs["split"], outs["unsplit"]):
+        assert rel_l2(host_f64(a), host_f64(b)) <= 2e-3
+    ws = torch.empty(base, dtype=torch.uint8, device="cuda")
+    g = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    st = capi.qat_attn_bwd(q, k, v, o_hp, lse, do, *g, B, H, Nq, Nkv, D, sc, 0, 1, ws, base - 1)
+    assert st == Status.WORKSPACE
+
+
 def test_expired_wait_is_reported_then_cleared():
     """The failure path of the kernels' bounded waits: the test entry waits on a barrier
     nothing arrives on, gives up after 50 ms and sets the device error word; the next
