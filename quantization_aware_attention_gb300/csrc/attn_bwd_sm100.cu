@@ -14,7 +14,10 @@
 // Kernels, in launch order on the caller's stream:
 //   bwd_prep_kernel       Delta and a copy of lse padded to 128-row blocks (+inf in the
 //                         padding, so P = 0 there).
-//   attn_bwd_dkdv_kernel  one CTA per SM, persistent over (head, 128-key block) items.
+//   attn_bwd_dkdv_kernel  one CTA per SM, persistent over (head, 128-key block) items;
+//                         with few such items, over (head, key block, query part)
+//                         items that store fp32 partial sums (bwd_key_split).
+//   bwd_part_sum_kernel   only then: adds the parts in order -> bf16 dV, dK.
 //   attn_bwd_dq_kernel    one CTA per SM, persistent over (head, 128-row query block).
 //
 // attn_bwd_dkdv_kernel, 352 threads:
@@ -40,7 +43,8 @@
 //   warps 3-10  two compute warpgroups, each owning 64 of a block's 128 query columns:
 //               P phase (P^T = exp2(qk_scale (S^T - lse / qk_scale)), bf16 over the
 //               group's S^T columns), dS phase (dS^T = P^T o (dP^T - Delta), bf16 over the
-//               group's dP^T columns), and per item one of dV / dK -> bf16 global.
+//               group's dP^T columns), and per item one of dV / dK -> bf16 global
+//               (fp32 partial sums in the workspace when the items are query parts).
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
 // Shared memory: K, V (one tile each), Q and dO (2 stages each, 128-byte swizzle), the
 // ones tile and the lse_ext / d_ext rows (128 x 16 bf16, 32-byte swizzle).
