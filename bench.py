@@ -277,7 +277,14 @@ def run_ours(args, w):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sm = w.sm_scale
-    launches_per_step = 4  # fwd kernel; bwd prep, dK/dV and dQ kernels
+    # fwd kernel; bwd prep, dK/dV and dQ kernels, plus the kernel that adds the dK/dV
+    # query parts when the backward splits its items (non-causal only; the workspace
+    # then ends with the parts' partial sums, past the 72 bytes per padded query row
+    # and the 4 KB ones tile of the unsplit layout)
+    rows_pad = B * H * ((Nq + 127) // 128 * 128)
+    up256 = lambda n: (n + 255) // 256 * 256
+    base_ws = 2 * up256(rows_pad * 4) + 2 * up256(rows_pad * 32) + up256(128 * 32)
+    launches_per_step = 4 + (1 if (not w.causal and ws_bytes > base_ws) else 0)
 
     def fwd():
         st = capi.qat_attn_fwd(x["q"], x["k"], x["v"], o_q, o_hp, lse, B, H, Nq, Nkv, D, sm,
