@@ -411,8 +411,6 @@ __global__ void __launch_bounds__(384, 1)
     };
     // P phase of block `blk` (global index c): P^T -> TMEM for the dV MMA
     auto p_phase = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
-      const uint32_t st = c & 1;
-      (void)st;
       if (!wwait(bar(B_S_FULL), c & 1)) return false;
       tc_fence_after();
       const bool diag = p.a.causal && blk == kb;
@@ -451,8 +449,6 @@ __global__ void __launch_bounds__(384, 1)
     const int pair = 2 * h + (quarter >> 1);
     const int wip = quarter & 1;
     auto p_phase_page = [&](uint32_t c, int blk, int kb, bool key_ok, int key) -> bool {
-      const uint32_t st = c & 1;
-      (void)st;
       if (!wwait(bar(B_S_FULL), c & 1)) return false;
       tc_fence_after();
       const bool diag = p.a.causal && blk == kb;

@@ -175,8 +175,6 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const int BH = p.a.B * p.a.H;
-  (void)BH;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
