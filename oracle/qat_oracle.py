@@ -47,9 +47,14 @@ CUDA kernels follow for one row x 64-key tile of fp32 probabilities:
 In exact arithmetic code depends only on p / amax, so it equals the definition above.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(closed forms, invariants, brute force, library routines, finite differences) except
-fidelity to the pages' own ``fake_quantize`` — parity unpinned, because its source
-(``quant_utils``) is not on the pages.
+(closed forms, invariants, brute force, library routines, finite differences):
+the bf16 conversions against torch's own conversions over tie, subnormal, overflow,
+infinity and NaN patterns; the page's backward through the closed forms its Delta
+source implies (dQ_page - dQ_ste = sm_scale c P K with c = <dO, O_hp - O_q>, torch
+autograd for the straight-through part) and the adjoint identity of its dV; the
+SMOOTH_K dQ term by the same closed forms.  The one exception is fidelity to the
+pages' own ``fake_quantize`` — parity unpinned, because its source (``quant_utils``)
+is not on the pages.
 """
 
 from __future__ import annotations
@@ -119,11 +124,19 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
 
 
 def f32_to_bf16_rn(x) -> np.ndarray:
-    """Round float32 values to bf16 (nearest, ties to even); returns float32 values."""
+    """Round float32 values to bf16 (nearest, ties to even); returns float32 values.
+
+    On the bit pattern u: adding 0x7FFF plus the lowest kept bit and truncating the low
+    16 bits rounds to nearest with ties to the even kept pattern; a carry out of the
+    mantissa raises the exponent (the largest finite values round up to infinity), and
+    infinities are unchanged.  NaN stays NaN: the carry could turn a NaN whose payload
+    sits in the low 16 bits into infinity, so NaNs take the quiet NaN of their sign.
+    """
     x = np.ascontiguousarray(x, dtype=np.float32)
     u = x.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    r = np.where(np.isnan(x), (u & 0x80000000) | 0x7FC00000, r)
+    return r.astype(np.uint32).view(np.float32)
 
 
 # ---------------------------------------------------------------------------
@@ -230,11 +243,24 @@ def forward(q, k, v, sm_scale: float, causal: bool, quant: bool, row_chunk: int 
 # Backward (fp64, straight-through estimator) for one (b, h) head
 # ---------------------------------------------------------------------------
 
-def head_backward(q, k, v, do, sm_scale: float, causal: bool):
+def _smooth_k_dq_term(ds, k_mean, sm_scale: float):
+    """The page's SMOOTH_K correction of dQ ("attn_qat_train.py", _attn_bwd_dq, the
+    ``if SMOOTH_K`` branch): every key block adds rowsum(dS) k_mean to dQ, so in all
+    sm_scale * rowsum_j(dS_ij) * k_mean.  K went into the scores with its channel mean
+    subtracted; the term gives dQ as if the mean had stayed in (dS (K + 1 k_mean^T))."""
+    if k_mean is None:
+        return 0.0
+    return sm_scale * ds.sum(axis=1)[:, None] * np.asarray(k_mean, np.float64)[None, :]
+
+
+def head_backward(q, k, v, do, sm_scale: float, causal: bool, k_mean=None):
     """Gradients of L = <dO, O_hp> with respect to q, k, v for one head (fp64).
 
     Delta_i = sum_d dO_id O_hp,id ; dP = dO V^T ; dS = P o (dP - Delta) ;
     dQ = sm_scale dS K ; dK = sm_scale dS^T Q ; dV = P^T dO.
+    With ``k_mean`` (smooth_k: K is the smoothed key) dQ also gets the page's SMOOTH_K
+    term sm_scale rowsum(dS) k_mean, which is zero in exact arithmetic here because
+    Delta comes from the same O_hp that P and V form.
     """
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
@@ -245,7 +271,8 @@ def head_backward(q, k, v, do, sm_scale: float, causal: bool):
     delta = (do * o_hp).sum(axis=1)
     dp = do @ v.T
     ds = p * (dp - delta[:, None])
-    return sm_scale * (ds @ k), sm_scale * (ds.T @ q), p.T @ do
+    dq = sm_scale * (ds @ k) + _smooth_k_dq_term(ds, k_mean, sm_scale)
+    return dq, sm_scale * (ds.T @ q), p.T @ do
 
 
 def backward(q, k, v, do, sm_scale: float, causal: bool):
@@ -407,8 +434,10 @@ def merge_partials(o_a, lse_a, o_b, lse_b):
 # o_for_bwd = O (the quantized output) to _attn_bwd_preprocess when use_high_prec_o is
 # False (its default), so Delta = rowsum(dO * O_q).
 
-def head_backward_page(q, k, v, do, sm_scale: float, causal: bool):
-    """dQ, dK, dV of the page's default backward for one head (fp64)."""
+def head_backward_page(q, k, v, do, sm_scale: float, causal: bool, k_mean=None):
+    """dQ, dK, dV of the page's default backward for one head (fp64).  With ``k_mean``
+    dQ gets the SMOOTH_K term, which is not zero here: sum_j dS_ij = Delta(O_hp)_i -
+    Delta(O_q)_i."""
     do = np.asarray(do, np.float64)
     f = head_forward(q, k, v, sm_scale, causal, quant=True, return_p=True)
     p, pq, o_q = f["p"], f["pq"], f["o_q"]
@@ -417,4 +446,48 @@ def head_backward_page(q, k, v, do, sm_scale: float, causal: bool):
     q = np.asarray(q, np.float64)
     delta = (do * o_q).sum(axis=1)
     ds = p * (do @ v.T - delta[:, None])
-    return sm_scale * (ds @ k), sm_scale * (ds.T @ q), pq.T @ do
+    dq = sm_scale * (ds @ k) + _smooth_k_dq_term(ds, k_mean, sm_scale)
+    return dq, sm_scale * (ds.T @ q), pq.T @ do
+
+
+def quant_rows_exact(p):
+    """Exact-arithmetic fake quantization of probabilities p [rows, Nkv] (fp64) per row x
+    absolute 64-key tile: code = E4M3(448 p / amax), value = code amax / 448; a tile with
+    amax = 0 stays zero.  (The same rule as the forward's, applied to a given P.)"""
+    p = np.asarray(p, np.float64)
+    out = np.zeros_like(p)
+    for lo in range(0, p.shape[1], QUANT_TILE):
+        t = p[:, lo:lo + QUANT_TILE]
+        amax = t.max(axis=1)
+        safe = np.where(amax > 0, amax, 1.0)
+        _, c = e4m3_rne_satfinite(E4M3_MAX * t / safe[:, None])
+        out[:, lo:lo + QUANT_TILE] = np.where((amax > 0)[:, None], c * (safe / E4M3_MAX)[:, None], 0.0)
+    return out
+
+
+def head_backward_from_stats(q, k, v, do, o, lse, sm_scale: float, causal: bool,
+                             quant_dv: bool = False, k_mean=None):
+    """The page's backward kernels taken literally for one head (fp64): P is
+    rematerialized from the SAVED base-2 lse ("attn_qat_train.py", _attn_bwd_dkdv and
+    _attn_bwd_dq: p = exp2(qk * qk_scale - m)), Delta from the given output o
+    (_attn_bwd_preprocess), dV from P or, with ``quant_dv``, from fake_quantize(P) per
+    query row x 64-key tile, and dQ with the SMOOTH_K term when ``k_mean`` is given.
+
+    When (o, lse) come from a forward on the same q, k, v this is ``head_backward``
+    (o = O_hp) or ``head_backward_page`` (o = O_q, quant_dv).  The page also runs it on
+    other inputs: with use_qat_qkv_backward = False the backward gets the unquantized
+    q, k, v while o and lse come from the forward on their fake-quantized copies, and
+    then the rows of P need not sum to 1."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    nq, nkv = q.shape[0], k.shape[0]
+    valid = _valid_mask(np.arange(nq), nkv, causal)
+    s = sm_scale * (q @ k.T)
+    p = np.where(valid, np.exp2(s / LN2 - np.asarray(lse, np.float64)[:, None]), 0.0)
+    delta = (do * np.asarray(o, np.float64)).sum(axis=1)
+    ds = p * (do @ v.T - delta[:, None])
+    dq = sm_scale * (ds @ k) + _smooth_k_dq_term(ds, k_mean, sm_scale)
+    pv = quant_rows_exact(p) if quant_dv else p
+    return dq, sm_scale * (ds.T @ q), pv.T @ do

@@ -432,3 +432,163 @@ def test_page_backward_terms():
     b = orc.head_backward(q, kk, v, do, sc, False)
     for x, y in zip(a, b):
         assert np.allclose(x, y, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- bf16 conversions vs torch
+
+def _torch_bf16_bits(x32: np.ndarray) -> np.ndarray:
+    """torch's own float32 -> bfloat16 conversion (a library routine), as bit patterns."""
+    t = torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_rounding_matches_torch():
+    """f32_to_bf16_rn against torch's conversion: exact ties with an even and an odd kept
+    bit, the neighbours of ties, subnormals, the largest finite values (which round to
+    infinity), signed zeros, infinities and NaNs."""
+    rng = np.random.default_rng(31)
+    hi = rng.integers(0, 1 << 16, 4000, dtype=np.uint64)
+    lows = np.array([0x0000, 0x0001, 0x7FFF, 0x8000, 0x8001, 0xFFFF], np.uint64)
+    pats = (hi[:, None] << 16 | lows[None, :]).ravel()
+    even_tie = (np.arange(0, 1 << 16, 2, dtype=np.uint64) << 16) | 0x8000   # kept bit 0
+    odd_tie = (np.arange(1, 1 << 16, 2, dtype=np.uint64) << 16) | 0x8000    # kept bit 1
+    special = np.array([0x00000000, 0x80000000, 0x00000001, 0x00008000, 0x00018000,
+                        0x007FFFFF, 0x807F8000, 0x7F7FFFFF, 0x7F7F7FFF, 0x7F7F8000,
+                        0xFF7FFFFF, 0x7F800000, 0xFF800000, 0x7FC00000, 0xFFC00000,
+                        0x7F800001, 0x7F807FFF, 0xFF800001, 0x7FFFFFFF], np.uint64)
+    u = np.concatenate([pats, even_tie, odd_tie, special]).astype(np.uint32)
+    x = u.view(np.float32)
+    got = (orc.f32_to_bf16_rn(x).view(np.uint32) >> 16).astype(np.uint16)
+    want = _torch_bf16_bits(x)
+    nan = np.isnan(x)
+    assert np.array_equal(got[~nan], want[~nan])
+    # NaN stays NaN with its sign (torch's NaN payload is its own choice)
+    g32 = (got[nan].astype(np.uint32) << 16).view(np.float32)
+    assert np.isnan(g32).all() and np.array_equal(np.signbit(g32), np.signbit(x[nan]))
+    # the finite tie cases really go to the even kept pattern, both ways (a carry out
+    # of the largest finite pattern gives infinity, as it should)
+    for ties, up in ((even_tie, 0), (odd_tie, 1)):
+        t32 = ties.astype(np.uint32).view(np.float32)
+        fin = np.isfinite(t32)
+        g = (orc.f32_to_bf16_rn(t32[fin]).view(np.uint32) >> 16).astype(np.uint64)
+        assert np.array_equal(g, (ties[fin] >> 16) + up)
+        assert fin.sum() > 32000
+
+
+def test_bf16_widening_matches_torch():
+    """bf16_bits_to_f64 against torch's bfloat16 -> float64 on every bit pattern."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):        # NaN patterns widen to NaN
+        got = orc.bf16_bits_to_f64(bits)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+# ---------------------------------------------------------------- Delta source and smooth_k
+
+def _torch_ste_grads(q, k, v, do, sc, causal):
+    """float64 autograd of <dO, softmax(sc Q K^T) V> (torch, a library routine)."""
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq[None, None], tk[None, None], tv[None, None], is_causal=causal, scale=sc)[0, 0]
+    (o * torch.tensor(do)).sum().backward()
+    return o.detach().numpy(), tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def _torch_softmax(q, k, sc, causal):
+    s = torch.tensor(q) @ torch.tensor(k).T * sc
+    if causal:
+        n = s.shape[0]
+        s = s.masked_fill(torch.ones(n, n, dtype=torch.bool).triu(1), float("-inf"))
+    return torch.softmax(s, dim=1).numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_page_backward_delta_source_closed_forms(causal):
+    """The page's backward forms Delta from O_q.  Then dS = dS_ste + c_i P_ij with
+    c_i = <dO_i, O_hp,i - O_q,i>, so against the straight-through gradients (torch
+    float64 autograd) dQ_page - dQ_ste = sm_scale c (P K) and dK_page - dK_ste =
+    sm_scale P^T diag(c) Q.  dV_page = Pq^T dO is pinned by its adjoint: for any V',
+    <dV_page, V'> = <dO, O_q(Q, K, V')>.  A Delta taken from O_hp, a dropped or
+    sign-flipped term, or a transposed dV product fails one of these."""
+    n, d, sc = 150, 8, 0.9
+    q, k, v, do = (rng_f64(200 + i, n, d, scale=1.5) for i in range(4))
+    dq, dk, dv = orc.head_backward_page(q, k, v, do, sc, causal)
+    o_hp, dq_s, dk_s, dv_s = _torch_ste_grads(q, k, v, do, sc, causal)
+    o_q = orc.head_forward(q, k, v, sc, causal, quant=True)["o_q"]
+    c = (do * (o_hp - o_q)).sum(axis=1)
+    assert np.abs(c).max() > 1e-3 * np.abs((do * o_hp).sum(axis=1)).max()  # O_q != O_hp
+    p = _torch_softmax(q, k, sc, causal)
+    assert np.allclose(dq - dq_s, sc * c[:, None] * (p @ k), rtol=1e-9, atol=1e-12)
+    assert np.allclose(dk - dk_s, sc * p.T @ (c[:, None] * q), rtol=1e-9, atol=1e-12)
+    v2 = rng_f64(209, n, d)
+    o_q2 = orc.head_forward(q, k, v2, sc, causal, quant=True)["o_q"]
+    assert np.isclose((dv * v2).sum(), (do * o_q2).sum(), rtol=1e-10)
+    assert not np.allclose(dq, dq_s, rtol=1e-4)   # the Delta source matters here
+
+
+def test_smooth_k_dq_term_closed_forms():
+    """SMOOTH_K adds sm_scale rowsum(dS) k_mean to dQ.  Straight-through: rowsum(dS) = 0,
+    and dQ equals torch's gradient through the unsmoothed K = K_s + k_mean.  The page's
+    backward: dQ = dQ_ste(K_s) + sm_scale c (P K_s + k_mean) with c as above."""
+    n, d, sc = 120, 8, 0.8
+    q, ks, v, do = (rng_f64(220 + i, n, d) for i in range(4))
+    mu = rng_f64(225, d, scale=3.0)
+    dq0, dk0, dv0 = orc.head_backward(q, ks, v, do, sc, False)
+    dq1, dk1, dv1 = orc.head_backward(q, ks, v, do, sc, False, k_mean=mu)
+    _, dq_t, _, _ = _torch_ste_grads(q, ks + mu[None, :], v, do, sc, False)
+    assert np.allclose(dq1, dq_t, rtol=1e-9, atol=1e-12)
+    assert np.allclose(dq1, dq0, rtol=1e-9, atol=1e-12)
+    assert np.array_equal(dk1, dk0) and np.array_equal(dv1, dv0)
+    dqp, dkp, dvp = orc.head_backward_page(q, ks, v, do, sc, False, k_mean=mu)
+    o_hp, dq_s, _, _ = _torch_ste_grads(q, ks, v, do, sc, False)
+    o_q = orc.head_forward(q, ks, v, sc, False, quant=True)["o_q"]
+    c = (do * (o_hp - o_q)).sum(axis=1)
+    p = _torch_softmax(q, ks, sc, False)
+    assert np.allclose(dqp, dq_s + sc * c[:, None] * (p @ ks + mu[None, :]), rtol=1e-9, atol=1e-12)
+    dqp0, dkp0, dvp0 = orc.head_backward_page(q, ks, v, do, sc, False)
+    assert np.array_equal(dkp, dkp0) and np.array_equal(dvp, dvp0)
+    assert not np.allclose(dqp, dqp0, rtol=1e-4)
+
+
+def test_quant_rows_exact_matches_forward_quantization():
+    """Quantizing the forward's P per row x tile gives the forward's Pq (the code depends
+    only on p / amax; the scale carries exp(T - m) / l); the codes are idempotent."""
+    n, d = 70, 8
+    q, k, v = (rng_f64(230 + i, n, d, scale=2.0) for i in range(3))
+    for causal in (False, True):
+        f = orc.head_forward(q, k, v, 0.7, causal, quant=True, return_p=True)
+        assert np.allclose(orc.quant_rows_exact(f["p"]), f["pq"], rtol=1e-12, atol=1e-15)
+    pq = orc.quant_rows_exact(f["p"])
+    assert np.allclose(orc.quant_rows_exact(pq), pq, rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_from_stats(causal):
+    """With (o, lse) from a forward on the same inputs the literal page form equals the
+    straight-through and the page's backward.  It rematerializes P from the SAVED lse:
+    shifting lse by an integer delta scales P by 2^-delta, and with o fixed every
+    gradient scales the same way, dV exactly so also when it is quantized (the E4M3 code
+    depends only on p / amax)."""
+    n, d, sc = 100, 8, 0.6
+    q, k, v, do = (rng_f64(240 + i, n, d) for i in range(4))
+    mu = rng_f64(245, d)
+    f = orc.head_forward(q, k, v, sc, causal, quant=True)
+    a = orc.head_backward_from_stats(q, k, v, do, f["o_hp"], f["lse"], sc, causal, k_mean=mu)
+    b = orc.head_backward(q, k, v, do, sc, causal, k_mean=mu)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-9, atol=1e-12)
+    a = orc.head_backward_from_stats(q, k, v, do, f["o_q"], f["lse"], sc, causal, quant_dv=True,
+                                     k_mean=mu)
+    b = orc.head_backward_page(q, k, v, do, sc, causal, k_mean=mu)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-9, atol=1e-12)
+    for qd in (False, True):
+        base = orc.head_backward_from_stats(q, k, v, do, f["o_q"], f["lse"], sc, causal, quant_dv=qd)
+        shift = orc.head_backward_from_stats(q, k, v, do, f["o_q"], f["lse"] + 3.0, sc, causal,
+                                             quant_dv=qd)
+        for x, y in zip(shift, base):
+            assert np.allclose(x, y / 8.0, rtol=1e-12, atol=1e-15)
