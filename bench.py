@@ -248,6 +248,69 @@ def run_reference(args, w):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+OTHER_WORKLOADS = ("c2", "c3", "c5a", "c5b")
+
+
+def time_workload(name, dev, stream, peaks, reps: int = 20, warmup: int = 3):
+    """qat_attn_fwd and qat_attn_bwd of one more workload, each timed alone with CUDA
+    events on the launching stream over `reps` warm repeats (median), inputs resident."""
+    import numpy as np
+    import torch
+
+    from quantization_aware_attention_gb300 import capi
+    from quantization_aware_attention_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[name]
+    B, H, Nq, Nkv, D = w.B, w.H, w.Nq, w.Nkv, w.D
+    x = {n: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+         for n, a in make_inputs(w).items()}
+    o_q, o_hp, dq = (torch.empty_like(x["q"]) for _ in range(3))
+    dk, dv = torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws_bytes = capi.qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    quant = capi.QUANT_P_FP8E4M3_ROW_TILE64
+
+    def fwd():
+        st = capi.qat_attn_fwd(x["q"], x["k"], x["v"], o_q, o_hp, lse, B, H, Nq, Nkv, D,
+                               w.sm_scale, int(w.causal), quant, stream)
+        if st != capi.Status.OK:
+            raise capi.QatError(st, "qat_attn_fwd")
+
+    def bwd():
+        st = capi.qat_attn_bwd(x["q"], x["k"], x["v"], o_hp, lse, x["do"], dq, dk, dv, B, H, Nq,
+                               Nkv, D, w.sm_scale, int(w.causal), quant, ws, ws_bytes, stream)
+        if st != capi.Status.OK:
+            raise capi.QatError(st, "qat_attn_bwd")
+
+    def timed(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    fwd_ms = timed(fwd)
+    bwd_ms = timed(bwd)
+    if capi.qat_attn_device_status(stream) != capi.Status.OK:
+        raise RuntimeError("a kernel reported an expired bounded wait")
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    fwd_tf = 6.0 * w.pairs * D / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = 10.0 * w.pairs * D / (bwd_ms * 1e-3) / 1e12
+    step_tf = 16.0 * w.pairs * D / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+    return {"shape": workload_config(w)["workload"], "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "step_tflops": step_tf,
+            "fwd_frac_of_burst_peak": fwd_tf / burst, "bwd_frac_of_burst_peak": bwd_tf / burst,
+            "tokens_per_s": B * Nq / ((fwd_ms + bwd_ms) * 1e-3), "reps": reps,
+            "l2": l2_note(w)}
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -485,6 +548,11 @@ def run_ours(args, w):
                    "what": "c4 forward as 4 key chunks (fp32 partials) + 3 lse merges"}
         del acc, part
 
+    # ---- the other workloads of the method (parity-test shapes, timed here too)
+    others = None
+    if w.name == WORKLOAD and not args.no_configs and world == 1:
+        others = {n: time_workload(n, dev, stream, load_peaks()[0]) for n in OTHER_WORKLOADS}
+
     # ---- roofline of the dominant kernel work (the backward call)
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -531,6 +599,7 @@ def run_ours(args, w):
                 peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))) if qkv else None,
             "kv_chunk_merge": dict(chunked, one_pass_fwd_ms=fwd_ms) if chunked else None},
         "clocks": clk,
+        "configs": others,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows, chunks = 2048, 4
@@ -559,6 +628,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads (c2, c3, c5a, c5b)")
     ap.add_argument("--shape", default=None,
                     help="B,H,Nq,Nkv,D[,causal]: a smaller case for profiling instead of the "
                          "benchmarked workload")

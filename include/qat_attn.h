@@ -144,6 +144,27 @@ QAT_API qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v,
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * qat_attn_bwd_smooth_k -- qat_attn_bwd for keys smoothed by smooth_k (the channel mean
+ * of K subtracted before attention, see qat_channel_mean): dQ also gets the page's
+ * SMOOTH_K term.  ("attn_qat_train.py", _attn_bwd_dq, the `if SMOOTH_K` branch: every key
+ * block adds rowsum(dS) k_mean to dq.)
+ *   k        the SMOOTHED keys the forward used (k - k_mean, or their fake-quantized copy)
+ *   k_mean   fp32 [D] (device, 16-byte aligned): the mean that was subtracted
+ *   dQ_i = sm_scale (sum_j dS_ij k_j + (sum_j dS_ij) k_mean), the fp32 dS summed over all
+ *   valid keys; dK and dV as qat_attn_bwd.  The term is zero in exact arithmetic under the
+ *   straight-through estimator (quant_mode 0 / 1: sum_j dS_ij = 0 when Delta comes from
+ *   O_hp) and not under quant_mode 2, where Delta comes from O_q.
+ *   Every other argument as qat_attn_bwd.
+ * Errors: as qat_attn_bwd; QAT_ERR_INVALID_ARG for a NULL or misaligned k_mean.
+ */
+QAT_API qat_status_t qat_attn_bwd_smooth_k(const void* q, const void* k, const void* v,
+                          const void* o_hp, const float* lse, const void* dO,
+                          void* dq, void* dk, void* dv, const float* k_mean,
+                          int B, int H, int Nq, int Nkv, int D,
+                          float sm_scale, int causal, int quant_mode,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * qat_attn_bwd_noalloc -- the same backward as qat_attn_bwd for callers that cannot
  * allocate device memory: for example a program whose device memory all belongs to
  * another runtime's pool, or one that must not allocate once running (an allocation
@@ -153,13 +174,15 @@ QAT_API qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v,
  *   in a fixed 32 MiB device array inside the library, held on every GPU that loads
  *   the library until the process exits.  It allocates nothing (no cudaMalloc,
  *   cudaFree or allocating library call).
- *   The first call on a device looks up that array's device address with the device
- *   current; make that first call before any stream capture.
+ *   Every call looks up that array's device address with the device current (a host-side
+ *   lookup that allocates nothing); the first call on a device also loads the library's
+ *   device code there, so make that first call before any stream capture.
  *   All calls share the array and it keeps the last call's contents; calls that overlap
  *   on the GPU race on it and must be ordered by the caller.
- * Errors: as qat_attn_bwd; QAT_ERR_WORKSPACE when the sizes need more scratch than the
- *   array holds, not counting the dK/dV partial sums (the workspace without them above
- *   32 MiB).  When the partial sums do not fit as well, the call runs without the split.
+ * Errors: as qat_attn_bwd, checked in the same order (sizes and modes, then pointers);
+ *   then QAT_ERR_WORKSPACE when the sizes need more scratch than the array holds, not
+ *   counting the dK/dV partial sums (the workspace without them above 32 MiB).  When the
+ *   partial sums do not fit as well, the call runs without the split.
  */
 QAT_API qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                           const void* o_hp, const float* lse, const void* dO,
@@ -234,6 +257,19 @@ QAT_API qat_status_t qat_fake_quant_tokens(const void* x, const float* mean, voi
                                            float* scales, int B, int H, int N, int D,
                                            void* stream);
 
+/*
+ * qat_subtract_mean -- out = bf16_RN(fl32(x - mean_c)): smooth_k's subtraction without the
+ * quantization.  The page's backward runs on the unquantized (but smoothed) keys when
+ * use_qat_qkv_backward is False ("attn_qat_train.py", _attention.forward keeps
+ * q_orig / k_orig / v_orig, taken after k = k - k_mean).
+ *   x     bf16 [B, H, N, D] (device)
+ *   mean  fp32 [D] (device, 16-byte aligned)
+ *   out   bf16 [B, H, N, D] OUT (may be x itself)
+ * Errors: QAT_ERR_INVALID_ARG (null / misaligned pointer, bad size or D), QAT_ERR_CUDA.
+ */
+QAT_API qat_status_t qat_subtract_mean(const void* x, const float* mean, void* out, int B, int H,
+                                       int N, int D, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 QAT_API const char* qat_status_string(qat_status_t status);
 
@@ -270,6 +306,21 @@ QAT_API qat_status_t qat_debug_quant_tiles(const float* p, int rows, int cols, f
  * Errors: QAT_ERR_INVALID_ARG (limit out of range), QAT_ERR_CUDA (launch error).
  */
 QAT_API qat_status_t qat_debug_wait_timeout(int limit_ms, void* stream);
+
+/*
+ * qat_debug_set_wait_limit_us -- test entry: sets the limit of the kernels' bounded waits
+ * on the current device (default 4,000,000 us = 4 s; 0 makes every wait that is not
+ * satisfied within its first few hundred polls expire).  With a lowered limit a real
+ * forward or backward gives up at its first slow wait: it sets the device error word,
+ * lets every copy and MMA it issued complete (those waits keep the 4 s limit), frees its
+ * TMEM and returns, leaving its outputs partly written; nothing faults or hangs.  The
+ * next qat_attn_device_status then reports QAT_ERR_TIMEOUT.  Synchronizes `stream` and
+ * the device first.  The page has no counterpart; this entry exists for the tests of the
+ * failure path.
+ *   limit_us  0 .. 4000000
+ * Errors: QAT_ERR_INVALID_ARG (limit out of range), QAT_ERR_CUDA.
+ */
+QAT_API qat_status_t qat_debug_set_wait_limit_us(int limit_us, void* stream);
 
 #ifdef __cplusplus
 }

@@ -393,6 +393,14 @@ def fake_quant_tokens_exact(x):
     return out
 
 
+def subtract_mean_bf16(x, mean):
+    """smooth_k's subtraction without the quantization, as stored: bf16_rn(fl32(x - mean))
+    per element (x float32 values [..., D], mean float32 [D]); returns float32 values."""
+    x = np.asarray(x, np.float32)
+    d = (x - np.asarray(mean, np.float32)).astype(np.float32)
+    return f32_to_bf16_rn(d)
+
+
 def channel_mean(x):
     """smooth_k's offset: the mean of x [B, H, N, D] over B, H and N, per channel (fp64)."""
     x = np.asarray(x, np.float64)

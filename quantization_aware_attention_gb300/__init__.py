@@ -8,5 +8,6 @@ and fails loudly if it has not been built.
 
 from .capi import (QUANT_NONE, QUANT_P_FP8E4M3_ROW_TILE64,  # noqa: F401
                    QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD, QatError, Status)
-from .attention import (QATAttention, attention, qat_attention_backward,  # noqa: F401
-                        qat_attention_forward, qat_prepare_qkv)
+from .attention import (QATAttention, attention, check_device_status,  # noqa: F401
+                        qat_attention_backward, qat_attention_forward, qat_prepare_qkv,
+                        qat_subtract_mean)

@@ -30,6 +30,9 @@ EXPORTED = (
     "qat_fake_quant_tokens",
     "qat_attn_fwd_chunk",
     "qat_attn_merge",
+    "qat_attn_bwd_smooth_k",
+    "qat_subtract_mean",
+    "qat_debug_set_wait_limit_us",
 )
 
 
@@ -90,6 +93,12 @@ def lib() -> ctypes.CDLL:
         L.qat_attn_fwd_chunk.restype = _i
         L.qat_attn_merge.argtypes = [_vp] * 8 + [_i] * 4 + [_vp]
         L.qat_attn_merge.restype = _i
+        L.qat_attn_bwd_smooth_k.argtypes = [_vp] * 10 + [_i] * 5 + [_f, _i, _i, _vp, _sz, _vp]
+        L.qat_attn_bwd_smooth_k.restype = _i
+        L.qat_subtract_mean.argtypes = [_vp] * 3 + [_i] * 4 + [_vp]
+        L.qat_subtract_mean.restype = _i
+        L.qat_debug_set_wait_limit_us.argtypes = [_i, _vp]
+        L.qat_debug_set_wait_limit_us.restype = _i
         _lib = L
     return _lib
 
@@ -140,6 +149,24 @@ def qat_attn_bwd_noalloc(q, k, v, o_hp, lse, dO, dq, dk, dv, B, H, Nq, Nkv, D, s
                                              _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Nq,
                                              Nkv, D, float(sm_scale), int(causal),
                                              int(quant_mode), _stream(stream)))
+
+
+def qat_attn_bwd_smooth_k(q, k, v, o_hp, lse, dO, dq, dk, dv, k_mean, B, H, Nq, Nkv, D, sm_scale,
+                          causal, quant_mode, workspace, workspace_bytes, stream=None) -> Status:
+    return Status(lib().qat_attn_bwd_smooth_k(_ptr(q), _ptr(k), _ptr(v), _ptr(o_hp), _ptr(lse),
+                                              _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                                              _ptr(k_mean), B, H, Nq, Nkv, D, float(sm_scale),
+                                              int(causal), int(quant_mode), _ptr(workspace),
+                                              int(workspace_bytes), _stream(stream)))
+
+
+def qat_subtract_mean(x, mean, out, B, H, N, D, stream=None) -> Status:
+    return Status(lib().qat_subtract_mean(_ptr(x), _ptr(mean), _ptr(out), B, H, N, D,
+                                          _stream(stream)))
+
+
+def qat_debug_set_wait_limit_us(limit_us, stream=None) -> Status:
+    return Status(lib().qat_debug_set_wait_limit_us(int(limit_us), _stream(stream)))
 
 
 def qat_attn_device_status(stream=None) -> Status:

@@ -9,6 +9,10 @@
 //   dS = P o (dP - Delta_i),  dQ += dS K_j       (dQ scaled by sm_scale at the end)
 // P is the unquantized probability in every quant mode: the straight-through estimator
 // passes the gradient of O_q through the quantizer as the identity.
+// With smooth_k's channel mean (BwdArgs::k_mean) dQ also gets the page's SMOOTH_K term
+// (_attn_bwd_dq, "if SMOOTH_K": dq += rowsum(ds) k_mean per key block): each thread sums
+// its fp32 dS over the item, the two warpgroups exchange their row sums through shared
+// memory, and the epilogue adds rowsum x k_mean before scaling.
 //
 // CTA layout (352 threads, one CTA per SM, persistent over (head, 128-row query block)):
 //   warp 0      TMA producer: the item's dO tile, then K_j (4-stage ring) and V_j
@@ -56,7 +60,8 @@ struct BwdDq {
   static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr uint32_t kOffMisc = kOffBar + 256;
-  static constexpr uint32_t kUsed = kOffMisc + 64;
+  static constexpr uint32_t kOffRs = kOffMisc + 64;       // dS row sums [2 groups][128]
+  static constexpr uint32_t kUsed = kOffRs + 2 * 128 * 4;
   // at least 116 KB so that no two CTAs share an SM (each holds all 512 TMEM columns)
   static constexpr uint32_t kSmemBytes = (kUsed + 1024 > 118784u ? kUsed + 1024 : 118784u);
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
@@ -69,7 +74,7 @@ enum : uint32_t {
   Q_K_FULL = 0, Q_K_EMPTY = Q_K_FULL + kKStages, Q_V_FULL = Q_K_EMPTY + kKStages,
   Q_V_EMPTY = Q_V_FULL + kVStages, Q_DO_FULL = Q_V_EMPTY + kVStages, Q_DO_EMPTY, Q_S_FULL,
   Q_S_EMPTY, Q_DP_FULL, Q_DP_EMPTY, Q_DS_FULL, Q_DS_FREE, Q_QR_FULL, Q_QR_EMPTY, Q_DQ_FULL,
-  Q_DQ_EMPTY, Q_DRAIN_A, Q_DRAIN_B, Q_COUNT
+  Q_DQ_EMPTY, Q_DRAIN_A, Q_DRAIN_B, Q_RS, Q_COUNT
 };
 static_assert(Q_COUNT <= 32, "barrier block");
 
@@ -134,7 +139,7 @@ __global__ void __launch_bounds__(384, 1)
     *abort_flag = 0;
     for (uint32_t i = 0; i < Q_COUNT; ++i) {
       const bool wg = i == Q_S_EMPTY || i == Q_DP_EMPTY || i == Q_DS_FULL || i == Q_QR_FULL ||
-                      i == Q_DQ_EMPTY;
+                      i == Q_DQ_EMPTY || i == Q_RS;
       mbar_init(bar(i), wg ? 256u : 1u);
     }
     fence_barrier_init();
@@ -190,11 +195,11 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       // drain: every issued load lands before the CTA exits
-      if (it > 0) mbar_wait(bar(Q_DO_FULL), (it - 1) & 1, abort_flag, p.err);
+      if (it > 0) mbar_wait_drain(bar(Q_DO_FULL), (it - 1) & 1, p.err);
       for (uint32_t i = (kc > kKStages ? kc - kKStages : 0); i < kc; ++i)
-        mbar_wait(bar(Q_K_FULL + i % kKStages), (i / kKStages) & 1, abort_flag, p.err);
+        mbar_wait_drain(bar(Q_K_FULL + i % kKStages), (i / kKStages) & 1, p.err);
       for (uint32_t i = (vc > kVStages ? vc - kVStages : 0); i < vc; ++i)
-        mbar_wait(bar(Q_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.err);
+        mbar_wait_drain(bar(Q_V_FULL + i % kVStages), (i / kVStages) & 1, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer A: S, dQ
@@ -258,7 +263,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (issued) {
         mma_commit(bar(Q_DRAIN_A));
-        mbar_wait(bar(Q_DRAIN_A), 0, abort_flag, p.err);
+        mbar_wait_drain(bar(Q_DRAIN_A), 0, p.err);
       }
     }
   } else if (warp == 2) {
@@ -295,7 +300,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (issued) {
         mma_commit(bar(Q_DRAIN_B));
-        mbar_wait(bar(Q_DRAIN_B), 0, abort_flag, p.err);
+        mbar_wait_drain(bar(Q_DRAIN_B), 0, p.err);
       }
     }
   } else {
@@ -305,6 +310,8 @@ __global__ void __launch_bounds__(384, 1)
     const int r = 32 * quarter + lane;               // query row of the block (TMEM lane)
     const uint32_t lrow = (32u * quarter) << 16;
     const float qk = p.a.qk_scale;
+    const bool smooth = p.a.k_mean != nullptr;
+    float* rsx = reinterpret_cast<float*>(gbase + C::kOffRs);  // [2 groups][128 rows]
     auto wwait = [&](uint32_t b_, uint32_t par) {
       const bool okw = mbar_wait(b_, par, abort_flag, p.err);
       return __all_sync(0xffffffffu, okw) != 0;
@@ -366,6 +373,7 @@ __global__ void __launch_bounds__(384, 1)
       // of block c - 1 has read the buffer.  dS_c is held in registers and written after
       // P of block c + 1 has been computed, so dQ_{c-1} has a block's time to complete.
       uint32_t pk[32];
+      float rs = 0.f;                                  // sum of this thread's fp32 dS
       auto write_ds = [&](uint32_t c) -> bool {
         if (c > 0 && !wwait(bar(Q_DS_FREE), (c - 1) & 1)) return false;
         tc_fence_after();
@@ -420,6 +428,7 @@ __global__ void __launch_bounds__(384, 1)
                 add_rn_f32x2(make_float2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])),
                              make_float2(-delta_r, -delta_r)));
             pk[16 * cc + i] = pack_bf16x2(d.x, d.y);
+            if (smooth) rs += d.x + d.y;
           }
         }
       }
@@ -437,6 +446,16 @@ __global__ void __launch_bounds__(384, 1)
       // ---- epilogue: group h stores dQ columns [hD/2, (h+1)D/2) of its row
       if (!(ok = wwait(bar(Q_DQ_FULL), it & 1))) break;
       tc_fence_after();
+      // SMOOTH_K: the row's dS sum over both groups' keys.  Written only after Q_DQ_FULL,
+      // which needs both groups' last dS of this item, so the other group has read the
+      // previous item's value by then.
+      float rowsum = 0.f;
+      if (smooth) {
+        rsx[h * 128 + r] = rs;
+        mbar_arrive(bar(Q_RS));
+        if (!(ok = wwait(bar(Q_RS), it & 1))) break;
+        rowsum = rsx[r] + rsx[128 + r];
+      }
       uint32_t o[D / 2];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
@@ -445,6 +464,17 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(Q_DQ_EMPTY));
+      if (smooth) {
+        const float4* km = reinterpret_cast<const float4*>(p.a.k_mean + (D / 2) * h);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const float4 m = km[c];
+          o[4 * c] = __float_as_uint(fmaf(rowsum, m.x, __uint_as_float(o[4 * c])));
+          o[4 * c + 1] = __float_as_uint(fmaf(rowsum, m.y, __uint_as_float(o[4 * c + 1])));
+          o[4 * c + 2] = __float_as_uint(fmaf(rowsum, m.z, __uint_as_float(o[4 * c + 2])));
+          o[4 * c + 3] = __float_as_uint(fmaf(rowsum, m.w, __uint_as_float(o[4 * c + 3])));
+        }
+      }
       if (row < p.a.Nq) {
         const float sc = p.a.sm_scale;
         uint4* dst = reinterpret_cast<uint4*>(p.a.dq + (static_cast<size_t>(bh) * p.a.Nq + row) * D +

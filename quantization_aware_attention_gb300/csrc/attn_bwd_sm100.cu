@@ -251,12 +251,12 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       // drain: every issued load lands before the CTA exits
-      if (it > 0) mbar_wait(bar(B_KV_FULL), (it - 1) & 1, abort_flag, p.err);
+      if (it > 0) mbar_wait_drain(bar(B_KV_FULL), (it - 1) & 1, p.err);
       for (uint32_t i = (qc > 2 ? qc - 2 : 0); i < qc; ++i)
-        mbar_wait(bar(B_Q_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
+        mbar_wait_drain(bar(B_Q_FULL0 + (i & 1)), (i >> 1) & 1, p.err);
       for (uint32_t i = (dc > 2 ? dc - 2 : 0); i < dc; ++i)
-        mbar_wait(bar(B_DO_FULL0 + (i & 1)), (i >> 1) & 1, abort_flag, p.err);
-      mbar_wait(bar(B_ONES_FULL), 0, abort_flag, p.err);
+        mbar_wait_drain(bar(B_DO_FULL0 + (i & 1)), (i >> 1) & 1, p.err);
+      mbar_wait_drain(bar(B_ONES_FULL), 0, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer A: S^T, dV
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (issued) {
         mma_commit(bar(B_DRAIN));
-        mbar_wait(bar(B_DRAIN), 0, abort_flag, p.err);
+        mbar_wait_drain(bar(B_DRAIN), 0, p.err);
       }
     }
   } else if (warp == 2) {
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (issued) {
         mma_commit(bar(B_DRAIN_B));
-        mbar_wait(bar(B_DRAIN_B), 0, abort_flag, p.err);
+        mbar_wait_drain(bar(B_DRAIN_B), 0, p.err);
       }
     }
   } else {

@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t kc = 0, vc = 0;
+      uint32_t kc = 0, vc = 0, qn = 0;  // K, V and Q loads issued
       int it = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(384, 1)
         const int J = kv_tiles(p, mt);
         ok = mbar_wait(bar(BAR_Q_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
         if (!ok) break;
+        ++qn;
         mbar_arrive_expect_tx(bar(BAR_Q_FULL), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(base + C::kOffQ + c * C::kChunkBytes, &tmQ, bar(BAR_Q_FULL), 64 * c,
@@ -217,11 +218,13 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      // drain: every issued load must land before the CTA can exit
+      // drain: every issued load must land before the CTA can exit (after an abort the
+      // score MMAs may not have waited for the last Q tile)
+      if (qn > 0) mbar_wait_drain(bar(BAR_Q_FULL), (qn - 1) & 1, p.err);
       for (uint32_t i = (kc > kKStages ? kc - kKStages : 0); i < kc; ++i)
-        mbar_wait(bar(BAR_K_FULL + i % kKStages), (i / kKStages) & 1, abort_flag, p.err);
+        mbar_wait_drain(bar(BAR_K_FULL + i % kKStages), (i / kKStages) & 1, p.err);
       for (uint32_t i = (vc > kVStages ? vc - kVStages : 0); i < vc; ++i)
-        mbar_wait(bar(BAR_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.err);
+        mbar_wait_drain(bar(BAR_V_FULL + i % kVStages), (i / kVStages) & 1, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ score MMAs (S = Q K^T)
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (issued) {  // drain: wait until every MMA this thread issued has completed
         mma_commit(bar(BAR_DRAIN));
-        mbar_wait(bar(BAR_DRAIN), 0, abort_flag, p.err);
+        mbar_wait_drain(bar(BAR_DRAIN), 0, p.err);
       }
     }
   } else if (warp == 2) {
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (issued) {
         mma_commit(bar(BAR_DRAIN_B));
-        mbar_wait(bar(BAR_DRAIN_B), 0, abort_flag, p.err);
+        mbar_wait_drain(bar(BAR_DRAIN_B), 0, p.err);
       }
     }
   } else {

@@ -3,9 +3,11 @@
 // the device-side error word.  No entry point here allocates device memory.
 #include "qat_attn.h"
 #include "qat_internal.h"
+#include "sm100.cuh"
 
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -14,22 +16,22 @@
 
 namespace qat {
 
-// Set by kernels whose bounded waits expire; read and cleared by qat_attn_device_status.
-__device__ unsigned int g_device_error = 0u;
+// The error word that kernels whose bounded waits expire set (read and cleared by
+// qat_attn_device_status), followed by the limit of those waits.
+__device__ sm100::DeviceState g_device_state = {0u, 0u, sm100::kWaitLimitNs};
 
 cudaError_t read_and_clear_device_error(unsigned int* out, cudaStream_t s) {
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return e;
-  e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(unsigned int));
+  e = cudaMemcpyFromSymbol(out, g_device_state, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
   const unsigned int zero = 0u;
-  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
+  return cudaMemcpyToSymbol(g_device_state, &zero, sizeof(unsigned int));
 }
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_ctx_mu;
-unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 }  // namespace
 
@@ -38,18 +40,19 @@ cudaError_t device_context(unsigned int** err, int* num_sms) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // a host-side lookup (no allocation), repeated on every call: a cached address would
+  // go stale when the device's context is destroyed and recreated
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_device_state);
+  if (e != cudaSuccess) return e;
+  *err = static_cast<unsigned int*>(p);
   std::lock_guard<std::mutex> lock(g_ctx_mu);
-  if (g_err_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_device_error);
-    if (e != cudaSuccess) return e;
+  if (g_num_sms[dev] == 0) {
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    g_err_ptr[dev] = static_cast<unsigned int*>(p);
     g_num_sms[dev] = n;
   }
-  *err = g_err_ptr[dev];
   *num_sms = g_num_sms[dev];
   return cudaSuccess;
 }
@@ -58,37 +61,12 @@ cudaError_t device_context(unsigned int** err, int* num_sms) {
 
 namespace {
 
+using qat::aligned16;
+using qat::check_sizes;
+using qat::kMaxRows;
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kAlign = 256;
-constexpr long long kMaxRows = 2147483647LL;  // rows of a [B*H*N, D] view
-constexpr int kMaxBH = 65535;                   // grid y dimension
-
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Checks shared by the forward and backward entry points.  Sets *empty when there is
-// no query work (B, H or Nq is zero).
-qat_status_t check_sizes(int B, int H, int Nq, int Nkv, int D, float sm_scale, int causal,
-                         int quant_mode, bool* empty) {
-  *empty = false;
-  if (B < 0 || H < 0 || Nq < 0 || Nkv < 0) return QAT_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return QAT_ERR_INVALID_ARG;
-  if (!(sm_scale > 0.f) || !isfinite(sm_scale)) return QAT_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return QAT_ERR_INVALID_ARG;
-  if (quant_mode != QAT_QUANT_NONE && quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64 &&
-      quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD)
-    return QAT_ERR_INVALID_ARG;
-  if (B == 0 || H == 0) {
-    *empty = true;
-    return QAT_OK;
-  }
-  if (Nkv < 1) return QAT_ERR_INVALID_ARG;
-  const long long bh = static_cast<long long>(B) * H;
-  if (bh * Nq > kMaxRows || bh * Nkv > kMaxRows) return QAT_ERR_INVALID_ARG;
-  if (bh > kMaxBH) return QAT_ERR_UNSUPPORTED;
-  if (causal && Nq != Nkv) return QAT_ERR_UNSUPPORTED;
-  if (Nq == 0) *empty = true;
-  return QAT_OK;
-}
 
 // With QAT_VERBOSE=1 in the environment, CUDA errors are also printed to stderr.
 qat_status_t from_cuda(cudaError_t e) {
@@ -213,11 +191,15 @@ size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D) {
   return qat::bwd_workspace_layout(B, H, Nq, Nkv, D, qat::bwd_key_split(B, H, Nq, Nkv)).total;
 }
 
-qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const void* o_hp,
-                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                          int B, int H, int Nq, int Nkv, int D, float sm_scale, int causal,
-                          int quant_mode, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+}  // extern "C"
+
+namespace {
+
+qat_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o_hp,
+                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                      const float* k_mean, int B, int H, int Nq, int Nkv, int D, float sm_scale,
+                      int causal, int quant_mode, void* workspace, size_t workspace_bytes,
+                      void* stream) {
   bool empty = false;
   const qat_status_t st = check_sizes(B, H, Nq, Nkv, D, sm_scale, causal, quant_mode, &empty);
   if (st != QAT_OK) return st;
@@ -261,6 +243,7 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.d_ext = reinterpret_cast<uint16_t*>(ws + wl.off_d_ext);
   a.ones = reinterpret_cast<uint16_t*>(ws + wl.off_ones);
   a.part = nsplit > 1 ? reinterpret_cast<float*>(ws + wl.off_part) : nullptr;
+  a.k_mean = k_mean;
   a.nsplit = nsplit;
   a.B = B; a.H = H; a.Nq = Nq; a.Nkv = Nkv; a.D = D;
   a.sm_scale = sm_scale;
@@ -271,6 +254,42 @@ qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const voi
   int num_sms = 0;
   cudaError_t e = qat::device_context(&err, &num_sms);
   if (e == cudaSuccess) e = qat::launch_bwd_tc(a, err, num_sms, s);
+  return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+qat_status_t qat_attn_bwd(const void* q, const void* k, const void* v, const void* o_hp,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          int B, int H, int Nq, int Nkv, int D, float sm_scale, int causal,
+                          int quant_mode, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  return bwd_impl(q, k, v, o_hp, lse, dO, dq, dk, dv, nullptr, B, H, Nq, Nkv, D, sm_scale,
+                  causal, quant_mode, workspace, workspace_bytes, stream);
+}
+
+qat_status_t qat_attn_bwd_smooth_k(const void* q, const void* k, const void* v,
+                                   const void* o_hp, const float* lse, const void* dO, void* dq,
+                                   void* dk, void* dv, const float* k_mean, int B, int H, int Nq,
+                                   int Nkv, int D, float sm_scale, int causal, int quant_mode,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (k_mean == nullptr || !aligned16(k_mean)) return QAT_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o_hp, lse, dO, dq, dk, dv, k_mean, B, H, Nq, Nkv, D, sm_scale,
+                  causal, quant_mode, workspace, workspace_bytes, stream);
+}
+
+qat_status_t qat_debug_set_wait_limit_us(int limit_us, void* stream) {
+  if (limit_us < 0 || limit_us > 4000000) return QAT_ERR_INVALID_ARG;
+  // no kernel of the library may be running while the limit changes
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  const unsigned long long ns =
+      limit_us == 0 ? 1ull : static_cast<unsigned long long>(limit_us) * 1000ull;
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbol(qat::g_device_state, &ns, sizeof(ns),
+                           offsetof(qat::sm100::DeviceState, wait_limit_ns));
   return from_cuda(e);
 }
 
@@ -310,6 +329,25 @@ qat_status_t qat_fake_quant_tokens(const void* x, const float* mean, void* out, 
   return from_cuda(qat::launch_fake_quant_tokens(
       static_cast<const uint16_t*>(x), mean, static_cast<uint16_t*>(out), scales,
       static_cast<int>(bh), N, D, static_cast<cudaStream_t>(stream)));
+}
+
+qat_status_t qat_subtract_mean(const void* x, const float* mean, void* out, int B, int H, int N,
+                               int D, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128)) return QAT_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows > kMaxRows) return QAT_ERR_INVALID_ARG;
+  if (rows == 0) return QAT_OK;
+  if (x == nullptr || out == nullptr || mean == nullptr || !aligned16(x) || !aligned16(out) ||
+      !aligned16(mean))
+    return QAT_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int num_sms = 0;
+  cudaError_t e = qat::device_context(&err, &num_sms);
+  if (e == cudaSuccess)
+    e = qat::launch_subtract_mean(static_cast<const uint16_t*>(x), mean,
+                                  static_cast<uint16_t*>(out), rows, D, num_sms,
+                                  static_cast<cudaStream_t>(stream));
+  return from_cuda(e);
 }
 
 qat_status_t qat_debug_quant_tiles(const float* p, int rows, int cols, float* deq, float* scales,

@@ -3,10 +3,43 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 
+#include "qat_attn.h"
+
 namespace qat {
+
+constexpr long long kMaxRows = 2147483647LL;  // rows of a [B*H*N, D] view
+constexpr int kMaxBH = 65535;                   // grid y dimension
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Size and mode checks shared by the forward and backward entry points.  Sets *empty
+// when there is no query work (B, H or Nq is zero).
+inline qat_status_t check_sizes(int B, int H, int Nq, int Nkv, int D, float sm_scale, int causal,
+                                int quant_mode, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || Nq < 0 || Nkv < 0) return QAT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return QAT_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !isfinite(sm_scale)) return QAT_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return QAT_ERR_INVALID_ARG;
+  if (quant_mode != QAT_QUANT_NONE && quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64 &&
+      quant_mode != QAT_QUANT_P_FP8E4M3_ROW_TILE64_PAGE_BWD)
+    return QAT_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) {
+    *empty = true;
+    return QAT_OK;
+  }
+  if (Nkv < 1) return QAT_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * Nq > kMaxRows || bh * Nkv > kMaxRows) return QAT_ERR_INVALID_ARG;
+  if (bh > kMaxBH) return QAT_ERR_UNSUPPORTED;
+  if (causal && Nq != Nkv) return QAT_ERR_UNSUPPORTED;
+  if (Nq == 0) *empty = true;
+  return QAT_OK;
+}
 
 // Backward workspace, each piece 256-byte aligned; query rows are padded per head to a
 // multiple of 128:
@@ -112,6 +145,7 @@ struct BwdArgs {
   uint16_t* d_ext;    // bf16 [B, H, Nq_pad, 16]
   uint16_t* ones;     // bf16 [128, 16]
   float* part;        // dK/dV partial sums (BwdWorkspace::off_part) when nsplit > 1
+  const float* k_mean;  // fp32 [D] or null: smooth_k's channel mean (dQ's SMOOTH_K term)
   int nsplit;         // query parts per dK/dV item: 1, or bwd_key_split(...) (non-causal)
   int B, H, Nq, Nkv, D;
   float sm_scale;
@@ -129,6 +163,8 @@ cudaError_t launch_channel_mean(const uint16_t* x, float* mean, long long rows, 
                                 int num_sms, cudaStream_t s);
 cudaError_t launch_fake_quant_tokens(const uint16_t* x, const float* mean, uint16_t* out,
                                      float* scales, int BH, int N, int D, cudaStream_t s);
+cudaError_t launch_subtract_mean(const uint16_t* x, const float* mean, uint16_t* out,
+                                 long long rows, int D, int num_sms, cudaStream_t s);
 cudaError_t launch_merge(float* o_q_acc, float* o_hp_acc, float* lse_acc, const float* o_q_part,
                          const float* o_hp_part, const float* lse_part, uint16_t* o_q_out,
                          uint16_t* o_hp_out, long long rows, int D, int num_sms, cudaStream_t s);
@@ -166,7 +202,9 @@ __device__ __forceinline__ void causal_item(int idx, int BH, int M, int hgroup, 
 
 // Device-side error word (bounded waits set it); defined in qat_api.cu.
 cudaError_t read_and_clear_device_error(unsigned int* out, cudaStream_t s);
-// Device address of that word and the SM count, for the current device (cached).
+// Device address of that word (the first member of the library's device state, looked
+// up on every call, so a context created after cudaDeviceReset gets its own) and the SM
+// count of the current device (cached).
 cudaError_t device_context(unsigned int** err, int* num_sms);
 
 }  // namespace qat

@@ -20,38 +20,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
-constexpr int kMaxDevices = 64;
 
 // The scratch.  In host code this name is only a stand-in for the device symbol: its
-// device address comes from cudaGetSymbolAddress, once per device.
+// device address comes from cudaGetSymbolAddress, with the device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up on the first
-// call on each device, with that device current).
+// Device address of the scratch array on the current device.  Looked up on every call (a
+// host-side table lookup that allocates nothing): a cached address would go stale if the
+// device's context were destroyed and recreated (cudaDeviceReset).  The first call on a
+// device loads the library's device code there.
 qat_status_t scratch_on_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QAT_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return QAT_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return QAT_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return QAT_ERR_CUDA;
+  *out = p;
   return QAT_OK;
 }
-
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -61,20 +48,24 @@ extern "C" qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const
                                              int B, int H, int Nq, int Nkv, int D,
                                              float sm_scale, int causal, int quant_mode,
                                              void* stream) {
-  // Invalid sizes, or no query rows: qat_attn_bwd validates and needs no scratch.
-  if (qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D) == 0 || B == 0 || H == 0 || Nq == 0)
+  // the same argument checks as qat_attn_bwd, in the same order, before the scratch size
+  bool empty = false;
+  const qat_status_t st = qat::check_sizes(B, H, Nq, Nkv, D, sm_scale, causal, quant_mode, &empty);
+  if (st != QAT_OK) return st;
+  // no query rows: qat_attn_bwd only zeroes dK and dV and needs no scratch
+  if (empty)
     return qat_attn_bwd(q, k, v, o_hp, lse, dO, dq, dk, dv, B, H, Nq, Nkv, D, sm_scale, causal,
                         quant_mode, nullptr, 0, stream);
+  const void* ptrs[] = {q, k, v, o_hp, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !qat::aligned16(p)) return QAT_ERR_INVALID_ARG;
   // the scratch must hold the workspace without the dK/dV query-part sums; qat_attn_bwd
   // uses the split only when those fit as well
   if (qat::bwd_workspace_layout(B, H, Nq, Nkv, D, 1).total > kNoAllocScratchBytes)
     return QAT_ERR_WORKSPACE;
-  const void* ptrs[] = {q, k, v, o_hp, lse, dO, dq, dk, dv};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned16(p)) return QAT_ERR_INVALID_ARG;
   void* scratch = nullptr;
-  const qat_status_t st = scratch_on_current_device(&scratch);
-  if (st != QAT_OK) return st;
+  const qat_status_t sst = scratch_on_current_device(&scratch);
+  if (sst != QAT_OK) return sst;
   return qat_attn_bwd(q, k, v, o_hp, lse, dO, dq, dk, dv, B, H, Nq, Nkv, D, sm_scale, causal,
                       quant_mode, scratch, kNoAllocScratchBytes, stream);
 }

@@ -1,6 +1,6 @@
 // qkv_quant.cu -- the page's IS_QAT input path: fake quantization of Q, K and V per
 // (head, 32-token block) to FP8 E4M3 with an absmax scale, and smooth_k's per-channel
-// mean of K over batch, heads and tokens.
+// mean of K over batch, heads and tokens, and that mean's subtraction alone.
 //
 // Sources ("attn_qat_train.py", _attention.forward): fake_quantize_q / fake_quantize_kv
 // run one program per 32-token block of one (batch, head); smooth_k subtracts
@@ -137,7 +137,47 @@ __global__ void __launch_bounds__(kThreads) fake_quant_tokens_kernel(
   }
 }
 
+// out = bf16_RN(fl32(x - mean_c)) for every element of a [rows, D] bf16 matrix: smooth_k's
+// subtraction without the quantization, for the page's backward on unquantized inputs
+// (use_qat_qkv_backward = False).  One thread per 8 elements (16-byte loads and stores).
+template <int D>
+__global__ void __launch_bounds__(256) subtract_mean_kernel(const uint16_t* __restrict__ x,
+                                                            const float* __restrict__ mean,
+                                                            uint16_t* __restrict__ out,
+                                                            long long n8) {
+  for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * 256) {
+    const int col = static_cast<int>(i % (D / 8)) * 8;
+    const uint4 raw = *reinterpret_cast<const uint4*>(x + i * 8);
+    const float4 m0 = *reinterpret_cast<const float4*>(mean + col);
+    const float4 m1 = *reinterpret_cast<const float4*>(mean + col + 4);
+    const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(b[k]);
+      __nv_bfloat162 r = __floats2bfloat162_rn(__fsub_rn(f.x, mm[2 * k]), __fsub_rn(f.y, mm[2 * k + 1]));
+      w[k] = *reinterpret_cast<uint32_t*>(&r);
+    }
+    *reinterpret_cast<uint4*>(out + i * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_subtract_mean(const uint16_t* x, const float* mean, uint16_t* out,
+                                 long long rows, int D, int num_sms, cudaStream_t s) {
+  const long long n8 = rows * D / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > static_cast<long long>(num_sms) * 32) blocks = static_cast<long long>(num_sms) * 32;
+  if (blocks == 0) return cudaSuccess;
+  if (D == 64)
+    subtract_mean_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, s>>>(x, mean, out, n8);
+  else
+    subtract_mean_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, s>>>(x, mean, out, n8);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_channel_mean(const uint16_t* x, float* mean, long long rows, int D,
                                 int num_sms, cudaStream_t s) {

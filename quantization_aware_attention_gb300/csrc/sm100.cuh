@@ -3,9 +3,12 @@
 // tensor core (tcgen05: TMEM allocation, MMA with fp32 accumulators in TMEM, commit to
 // mbarrier, TMEM <-> register moves).
 //
-// Every wait on an mbarrier is bounded: after kWaitLimitNs of spinning the waiter sets
-// the library's device error word and a CTA-local abort flag and returns false, so a
-// lost arrival ends the kernel with an error status instead of hanging the GPU.
+// Every wait on an mbarrier is bounded: after the device state's wait limit (4 s unless
+// a test entry lowered it) the waiter sets the library's device error word and a
+// CTA-local abort flag and returns false, so a lost arrival ends the kernel with an
+// error status instead of hanging the GPU.  Before it exits, a kernel waits for the
+// asynchronous copies and MMAs it has issued (mbar_wait_drain), which complete on their
+// own; those waits ignore the abort flag and the lowered limit.
 #pragma once
 
 #include <cuda.h>
@@ -15,6 +18,18 @@ namespace qat {
 namespace sm100 {
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
+
+// The library's per-device state (defined in qat_api.cu).  Kernels receive a pointer to
+// its first member, the error word, and read the wait limit that follows it.
+struct DeviceState {
+  unsigned int error;                // bit 0 set by a wait that expired
+  unsigned int reserved;
+  unsigned long long wait_limit_ns;  // limit of the abortable waits
+};
+
+__device__ __forceinline__ unsigned long long state_wait_limit(const unsigned int* err) {
+  return reinterpret_cast<const volatile DeviceState*>(err)->wait_limit_ns;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -60,21 +75,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the phase with parity `parity` of `bar` has completed.  Returns false if
-// the CTA is aborting or the wait exceeded `limit_ns` (then the error word is set).
+// the CTA is aborting or the wait exceeded its limit (then the error word is set): an
+// explicit `limit_ns`, else the device state's.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* err,
-                                          unsigned long long limit_ns = kWaitLimitNs) {
+                                          unsigned int* err, unsigned long long limit_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0u) {
       if (*abort_flag) return false;
+      if (limit_ns == 0) limit_ns = state_wait_limit(err);
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(err, 1u);
         return false;
       }
+    }
+  }
+}
+
+// Waits for the completion of a copy or MMA this CTA issued, before the CTA frees TMEM or
+// exits: such work completes by itself, so the wait ignores the abort flag and the
+// lowered limit and gives up (setting the error word) only after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, 1u);
+      return false;
     }
   }
 }

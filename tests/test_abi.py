@@ -142,3 +142,46 @@ def test_chunk_and_merge_validation():
     assert capi.qat_attn_merge(A, A, None, A, A, A, None, None, 1, 1, 8, 128, 0) == Status.INVALID_ARG
     assert capi.qat_attn_merge(A, A, A, A, A, A, None, None, 1, 1, 8, 96, 0) == Status.INVALID_ARG
     assert capi.qat_attn_merge(None, None, None, None, None, None, None, None, 0, 1, 8, 128, 0) == Status.OK
+
+
+def noalloc(**kw):
+    args = dict(q=A, k=A, v=A, o_hp=A, lse=A, dO=A, dq=A, dk=A, dv=A, B=1, H=128, Nq=65537,
+                Nkv=65537, D=128, sm_scale=0.088, causal=0, quant_mode=1, stream=0)
+    args.update(kw)
+    return capi.qat_attn_bwd_noalloc(**args)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(), Status.WORKSPACE),                       # valid, but its scratch would not fit
+    (dict(causal=1, Nkv=65536), Status.UNSUPPORTED),  # argument errors come first, as in
+    (dict(sm_scale=-1.0), Status.INVALID_ARG),        # qat_attn_bwd
+    (dict(quant_mode=5), Status.INVALID_ARG),
+    (dict(D=80), Status.INVALID_ARG),
+    (dict(dv=None), Status.INVALID_ARG),
+    (dict(q=A + 8), Status.INVALID_ARG),
+    (dict(H=0, q=None), Status.OK),
+    (dict(Nq=0, dk=None), Status.INVALID_ARG),
+])
+def test_noalloc_validation_order(kw, want):
+    """The no-alloc backward checks its arguments exactly as qat_attn_bwd does, before the
+    size of its fixed scratch: an oversize call with a bad mode or shape reports that."""
+    assert noalloc(**kw) == want
+
+
+def test_smooth_k_backward_validation():
+    args = dict(q=A, k=A, v=A, o_hp=A, lse=A, dO=A, dq=A, dk=A, dv=A, k_mean=A, B=1, H=1, Nq=8,
+                Nkv=8, D=64, sm_scale=0.125, causal=0, quant_mode=2, workspace=None,
+                workspace_bytes=0, stream=0)
+    assert capi.qat_attn_bwd_smooth_k(**{**args, "k_mean": None}) == Status.INVALID_ARG
+    assert capi.qat_attn_bwd_smooth_k(**{**args, "k_mean": A + 4}) == Status.INVALID_ARG
+    assert capi.qat_attn_bwd_smooth_k(**args) == Status.WORKSPACE
+    assert capi.qat_attn_bwd_smooth_k(**{**args, "D": 96}) == Status.INVALID_ARG
+
+
+def test_subtract_mean_and_wait_limit_validation():
+    assert capi.qat_subtract_mean(A, A, A, 1, 1, 8, 96, stream=0) == Status.INVALID_ARG
+    assert capi.qat_subtract_mean(A, None, A, 1, 1, 8, 64, stream=0) == Status.INVALID_ARG
+    assert capi.qat_subtract_mean(A, A + 4, A, 1, 1, 8, 64, stream=0) == Status.INVALID_ARG
+    assert capi.qat_subtract_mean(None, None, None, 0, 1, 8, 64, stream=0) == Status.OK
+    assert capi.qat_debug_set_wait_limit_us(-1, stream=0) == Status.INVALID_ARG
+    assert capi.qat_debug_set_wait_limit_us(4000001, stream=0) == Status.INVALID_ARG

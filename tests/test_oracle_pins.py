@@ -592,3 +592,14 @@ def test_backward_from_stats(causal):
                                              quant_dv=qd)
         for x, y in zip(shift, base):
             assert np.allclose(x, y / 8.0, rtol=1e-12, atol=1e-15)
+
+
+def test_subtract_mean_bf16_matches_torch():
+    """bf16(fl32(x - mean)) against torch's float32 subtraction and bf16 conversion."""
+    rng = np.random.default_rng(250)
+    x = orc.f32_to_bf16_rn(rng.standard_normal((40, 64)).astype(np.float32) * 3)
+    mu = (rng.standard_normal(64) * 2).astype(np.float32)
+    got = orc.subtract_mean_bf16(x, mu)
+    want = (torch.from_numpy(x) - torch.from_numpy(mu)).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(got, want)
+    assert np.array_equal(orc.subtract_mean_bf16(x, np.zeros(64, np.float32)), x)
