@@ -130,13 +130,13 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 8);
+  volatile WaitCtl* abort_flag = reinterpret_cast<volatile WaitCtl*>(gbase + C::kOffMisc + 8);
   const uint32_t bars = base + C::kOffBar;
   auto bar = [&](uint32_t i) { return bars + 8u * i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    *abort_flag = 0;
+    wait_ctl_init(abort_flag, p.err);
     for (uint32_t i = 0; i < Q_COUNT; ++i) {
       const bool wg = i == Q_S_EMPTY || i == Q_DP_EMPTY || i == Q_DS_FULL || i == Q_QR_FULL ||
                       i == Q_DQ_EMPTY || i == Q_RS;

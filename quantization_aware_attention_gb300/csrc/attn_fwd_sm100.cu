@@ -137,12 +137,12 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + C::kOffBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 8);
+  volatile WaitCtl* abort_flag = reinterpret_cast<volatile WaitCtl*>(gbase + C::kOffMisc + 8);
   auto bar = [&](uint32_t i) { return bars + 8u * i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    *abort_flag = 0;
+    wait_ctl_init(abort_flag, p.err);
     mbar_init(bar(BAR_Q_FULL), 1);
     mbar_init(bar(BAR_Q_EMPTY), 1);
     for (int s = 0; s < kKStages; ++s) {

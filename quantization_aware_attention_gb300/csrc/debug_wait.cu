@@ -15,13 +15,14 @@ using namespace sm100;
 __global__ void __launch_bounds__(32) wait_timeout_kernel(unsigned int* err,
                                                           unsigned long long limit_ns) {
   __shared__ __align__(8) unsigned long long bar_word;
-  __shared__ int abort_word;
+  __shared__ WaitCtl ctl;
   if (threadIdx.x == 0) {
-    abort_word = 0;
+    ctl.abort = 0;
+    ctl.limit_ns = limit_ns;
     mbar_init(smem_addr(&bar_word), 1);
     fence_barrier_init();
     // phase 0 of a fresh barrier completes only after one arrival, and none comes
-    mbar_wait(smem_addr(&bar_word), 0, &abort_word, err, limit_ns);
+    mbar_wait(smem_addr(&bar_word), 0, &ctl, err, limit_ns);
   }
 }
 

@@ -3,8 +3,8 @@
 // tensor core (tcgen05: TMEM allocation, MMA with fp32 accumulators in TMEM, commit to
 // mbarrier, TMEM <-> register moves).
 //
-// Every wait on an mbarrier is bounded: after the device state's wait limit (4 s unless
-// a test entry lowered it) the waiter sets the library's device error word and a
+// Every wait on an mbarrier is bounded: after the wait limit (the device state's, 4 s
+// unless a test entry lowered it) the waiter sets the library's device error word and a
 // CTA-local abort flag and returns false, so a lost arrival ends the kernel with an
 // error status instead of hanging the GPU.  Before it exits, a kernel waits for the
 // asynchronous copies and MMAs it has issued (mbar_wait_drain), which complete on their
@@ -30,6 +30,24 @@ struct DeviceState {
 __device__ __forceinline__ unsigned long long state_wait_limit(const unsigned int* err) {
   return reinterpret_cast<const volatile DeviceState*>(err)->wait_limit_ns;
 }
+
+// Per-CTA wait control in shared memory: the abort flag an expired wait raises for the
+// whole CTA, and the wait limit, copied from the device state when the kernel starts so
+// that waits read it from shared memory.
+struct WaitCtl {
+  int abort;
+  int reserved;
+  unsigned long long limit_ns;
+};
+
+// One thread, before the CTA's first __syncthreads.
+__device__ __forceinline__ void wait_ctl_init(volatile WaitCtl* w, const unsigned int* err) {
+  w->abort = 0;
+  w->limit_ns = state_wait_limit(err);
+}
+
+// A limit below this one (only a test entry sets such) is checked on every poll.
+constexpr unsigned long long kShortLimitNs = 1000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -76,18 +94,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits until the phase with parity `parity` of `bar` has completed.  Returns false if
 // the CTA is aborting or the wait exceeded its limit (then the error word is set): an
-// explicit `limit_ns`, else the device state's.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+// explicit `limit_ns`, else the CTA's copy of the device state's.  The abort flag and the
+// clock are checked every 256 polls (a try_wait suspends the thread for a while), or on
+// every poll under a test's short limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile WaitCtl* ctl,
                                           unsigned int* err, unsigned long long limit_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
+  if (limit_ns == 0) limit_ns = ctl->limit_ns;
+  const bool every = limit_ns < kShortLimitNs;
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u) {
-      if (*abort_flag) return false;
-      if (limit_ns == 0) limit_ns = state_wait_limit(err);
+    if (every || (i & 255u) == 0u) {
+      if (ctl->abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
+        ctl->abort = 1;
         atomicOr(err, 1u);
         return false;
       }
