@@ -577,9 +577,10 @@ def run_ours(args, w):
             "kernel": "qat_attn_bwd call (prep + attn_bwd_dkdv_kernel + attn_bwd_dq_kernel)",
             "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
             "frac": bwd_tf / peak_sus,
-            "traffic": (kernel_traffic("attn_bwd_dkdv_kernel", "attn_bwd_dq_kernel")
+            "traffic": (kernel_traffic("bwd_prep_kernel", "attn_bwd_dkdv_kernel",
+                                       "attn_bwd_dq_kernel")
                         if w.name == WORKLOAD else None),
-            "traffic_unit": "bytes per qat_attn_bwd call: its dK/dV and dQ kernels (DRAM read + write)",
+            "traffic_unit": "bytes per qat_attn_bwd call: its prep, dK/dV and dQ kernels (DRAM read + write)",
             "peak_kind": f"bf16_tflops_sustained ({peak_src})",
             "algorithmic_flops_per_launch": 10.0 * pairs * D,
             # what the tensor cores execute: S and dP in both kernels (7 products) and the

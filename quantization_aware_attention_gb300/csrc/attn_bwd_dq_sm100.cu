@@ -119,7 +119,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Bounds of 384 threads cap registers at 168 per thread: with 11 warps, three share a
 // sub-partition's 16K registers, so a 352-thread CTA cannot launch with more.
-template <int D>
+// kSmooth: a k_mean is passed (the SMOOTH_K term); a separate instance, so that the
+// hot loop of the plain backward carries no row-sum register or add.
+template <int D, bool kSmooth>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -310,7 +312,6 @@ __global__ void __launch_bounds__(384, 1)
     const int r = 32 * quarter + lane;               // query row of the block (TMEM lane)
     const uint32_t lrow = (32u * quarter) << 16;
     const float qk = p.a.qk_scale;
-    const bool smooth = p.a.k_mean != nullptr;
     float* rsx = reinterpret_cast<float*>(gbase + C::kOffRs);  // [2 groups][128 rows]
     auto wwait = [&](uint32_t b_, uint32_t par) {
       const bool okw = mbar_wait(b_, par, abort_flag, p.err);
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(384, 1)
                 add_rn_f32x2(make_float2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])),
                              make_float2(-delta_r, -delta_r)));
             pk[16 * cc + i] = pack_bf16x2(d.x, d.y);
-            if (smooth) rs += d.x + d.y;
+            if constexpr (kSmooth) rs += d.x + d.y;
           }
         }
       }
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(384, 1)
       // which needs both groups' last dS of this item, so the other group has read the
       // previous item's value by then.
       float rowsum = 0.f;
-      if (smooth) {
+      if constexpr (kSmooth) {
         rsx[h * 128 + r] = rs;
         mbar_arrive(bar(Q_RS));
         if (!(ok = wwait(bar(Q_RS), it & 1))) break;
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(Q_DQ_EMPTY));
-      if (smooth) {
+      if constexpr (kSmooth) {
         const float4* km = reinterpret_cast<const float4*>(p.a.k_mean + (D / 2) * h);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -512,12 +513,12 @@ cudaError_t launch_bwd_dq_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   if (!make_bf16_map_3d(&mk, a.k, D, a.Nkv, BH) || !make_bf16_map_3d(&mv, a.v, D, a.Nkv, BH) ||
       !make_bf16_map_3d(&mdo, a.dO, D, a.Nq, BH))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = a.k_mean != nullptr ? attn_bwd_dq_kernel<D, true> : attn_bwd_dq_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = p.items < num_sms ? p.items : num_sms;
-  attn_bwd_dq_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mk, mv, mdo, p);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mk, mv, mdo, p);
   return cudaGetLastError();
 }
 
