@@ -102,6 +102,14 @@ __device__ __forceinline__ void dq_item(int idx, const DqParams& p, int& bh, int
   }
 }
 
+// 32 bytes from global memory (32-byte aligned) into r[0..7]
+__device__ __forceinline__ void load32(const uint16_t* ptr, uint32_t* r) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(ptr));
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
@@ -318,20 +326,31 @@ __global__ void __launch_bounds__(384, 1)
       return __all_sync(0xffffffffu, okw) != 0;
     };
     // half h of this thread's Q row into TMEM as bf16 pairs (D / 4 columns); rows past Nq
-    // are zero (their lse is +inf, so P = 0 there)
+    // are zero (their lse is +inf, so P = 0 there).  Each thread reads a different row,
+    // so one load instruction touches 32 lines; with a 32-byte aligned q the rows are
+    // read 32 bytes at a time.
+    const bool q32 = (reinterpret_cast<uintptr_t>(p.a.q) & 31u) == 0;
     auto load_q = [&](int bh, int mt) {
       constexpr int kCols = D / 4;
       const int row = mt * kBlk + r;
       const uint16_t* src = p.a.q + (static_cast<size_t>(bh) * p.a.Nq + row) * D + (D / 2) * h;
       uint32_t v[kCols];
 #pragma unroll
-      for (int u = 0; u < kCols / 4; ++u) {
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (row < p.a.Nq) x = *reinterpret_cast<const uint4*>(src + 8 * u);
-        v[4 * u] = x.x;
-        v[4 * u + 1] = x.y;
-        v[4 * u + 2] = x.z;
-        v[4 * u + 3] = x.w;
+      for (int u = 0; u < kCols; ++u) v[u] = 0u;
+      if (row < p.a.Nq) {
+        if (q32) {  // 32-byte loads: half the L1 wavefronts of 16-byte ones for these rows
+#pragma unroll
+          for (int u = 0; u < kCols / 8; ++u) load32(src + 16 * u, &v[8 * u]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < kCols / 4; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + 8 * u);
+            v[4 * u] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
+          }
+        }
       }
       const uint32_t dst = tbase + lrow + C::kTmemQ + kCols * h;
       if constexpr (kCols == 32)
@@ -345,20 +364,27 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t bc = 0;
     int it = 0;
     bool ok = true;
+    // lse and Delta of this thread's row in the next item, read with its Q rows
+    float lse_n = 0.f, delta_n = 0.f;
+    auto load_next = [&](int bh, int mt) {
+      load_q(bh, mt);
+      const size_t prow = static_cast<size_t>(bh) * p.nq_pad + mt * kBlk + r;
+      lse_n = p.a.lse_pad[prow];
+      delta_n = p.a.delta[prow];
+    };
     if (static_cast<int>(blockIdx.x) < p.items) {
       int bh, mt, J;
       dq_item(blockIdx.x, p, bh, mt, J);
-      load_q(bh, mt);
+      load_next(bh, mt);
     }
     for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
       int bh, mt, J;
       dq_item(idx, p, bh, mt, J);
       const int row = mt * kBlk + r;
-      const size_t prow = static_cast<size_t>(bh) * p.nq_pad + row;
-      const float lse_r = p.a.lse_pad[prow];
-      const float delta_r = p.a.delta[prow];
-      {  // the next item's Q half-row, lse and Delta, read at its start, into L2 now
-        const int nidx = idx + static_cast<int>(gridDim.x);
+      const float lse_r = lse_n;
+      const float delta_r = delta_n;
+      const int nidx = idx + static_cast<int>(gridDim.x);
+      {  // the next item's Q half-row, lse and Delta, read during this item, into L2 now
         if (nidx < p.items) {
           int nbh, nmt, nJ;
           dq_item(nidx, p, nbh, nmt, nJ);
@@ -436,13 +462,12 @@ __global__ void __launch_bounds__(384, 1)
       if (ok) ok = write_ds(bc - 1);   // the item's last dS
       if (!ok) break;
       // the next item's Q rows go in once this item's last S has read the current ones
-      const int nidx = idx + static_cast<int>(gridDim.x);
       if (nidx < p.items) {
         if (!(ok = wwait(bar(Q_QR_EMPTY), it & 1))) break;
         tc_fence_after();
         int nbh, nmt, nJ;
         dq_item(nidx, p, nbh, nmt, nJ);
-        load_q(nbh, nmt);
+        load_next(nbh, nmt);
       }
       // ---- epilogue: group h stores dQ columns [hD/2, (h+1)D/2) of its row
       if (!(ok = wwait(bar(Q_DQ_FULL), it & 1))) break;
