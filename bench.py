@@ -353,9 +353,9 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     sm = w.sm_scale
     # fwd kernel; bwd prep, dK/dV and dQ kernels, plus the kernel that adds the dK/dV
-    # query parts when the backward splits its items (non-causal only; the workspace
-    # then ends with the parts' partial sums, past the 72 bytes per padded query row
-    # and the 4 KB ones tile of the unsplit layout)
+    # segment sums when the backward runs stream-K (non-causal only; the workspace then
+    # ends with the segments' partial sums, past the 72 bytes per padded query row and
+    # the 4 KB ones tile of the unsplit layout)
     rows_pad = B * H * ((Nq + 127) // 128 * 128)
     up256 = lambda n: (n + 255) // 256 * 256
     base_ws = 2 * up256(rows_pad * 4) + 2 * up256(rows_pad * 32) + up256(128 * 32)

@@ -101,11 +101,12 @@ QAT_API qat_status_t qat_attn_fwd(const void* q, const void* k, const void* v,
  * -lse / (sm_scale log2 e) and -Delta, each as a sum of three bf16 terms, which the
  * dK/dV kernel adds to its score products through one extra MMA step; and a 4 KB
  * bf16 ones tile.  About 72 bytes per padded query row.  When the sizes give few
- * (head, 128-key block) pairs for the GPU's SMs, the dK/dV kernel splits each pair's
- * query blocks into parts and the workspace also holds the parts' fp32 partial sums of
- * dV and dK: parts x 2 x B x H x Nkv x D x 4 bytes (4 parts at B1 H40 Nq16384 Nkv512,
- * 84 MB).  The rule depends on the sizes only; it is also applied for causal calls,
- * which do not split, so a causal caller may get more workspace than it uses.
+ * (head, 128-key block) pairs for the GPU's SMs, the dK/dV kernel cuts the pairs' query
+ * blocks into one equal range per CTA (stream-K) and the workspace also holds fp32
+ * partial sums of dV and dK for the pairs the ranges cut: two 128-row slots per CTA,
+ * CTAs x 2 x 2 x 128 x D x 4 bytes (152 CTAs at B1 H40 Nq16384 Nkv512 D128, 40 MB).
+ * The rule depends on the sizes only; it is also applied for causal calls, which do
+ * not split, so a causal caller may get more workspace than it uses.
  * Returns 0 for invalid sizes.  Host-only; never touches the device.
  */
 QAT_API size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D);
@@ -131,7 +132,8 @@ QAT_API size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D
  *              256-byte aligned, owned by the caller; its contents on entry are
  *              ignored and on exit unspecified.
  *              A buffer that holds everything but the dK/dV partial sums (see
- *              qat_attn_bwd_workspace_bytes) is accepted and runs without the split.
+ *              qat_attn_bwd_workspace_bytes) is accepted and runs with one CTA per
+ *              (head, key block) pair instead.
  * Errors: as qat_attn_fwd, plus QAT_ERR_WORKSPACE when workspace is NULL or
  *   workspace_bytes is below the workspace without the partial sums.  Nq == 0 with
  *   Nkv >= 1 writes zero dk, dv.
@@ -182,7 +184,7 @@ QAT_API qat_status_t qat_attn_bwd_smooth_k(const void* q, const void* k, const v
  * Errors: as qat_attn_bwd, checked in the same order (sizes and modes, then pointers);
  *   then QAT_ERR_WORKSPACE when the sizes need more scratch than the array holds, not
  *   counting the dK/dV partial sums (the workspace without them above 32 MiB).  When the
- *   partial sums do not fit as well, the call runs without the split.
+ *   partial sums do not fit as well, the call runs with one CTA per (head, key block).
  */
 QAT_API qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                           const void* o_hp, const float* lse, const void* dO,

@@ -15,9 +15,10 @@
 //   bwd_prep_kernel       Delta and a copy of lse padded to 128-row blocks (+inf in the
 //                         padding, so P = 0 there).
 //   attn_bwd_dkdv_kernel  one CTA per SM, persistent over (head, 128-key block) items;
-//                         with few such items, over (head, key block, query part)
-//                         items that store fp32 partial sums (bwd_key_split).
-//   bwd_part_sum_kernel   only then: adds the parts in order -> bf16 dV, dK.
+//                         with few such items (non-causal), over equal ranges of the
+//                         items' query blocks, whose cut items store fp32 partial sums
+//                         (stream-K, bwd_stream_k_ctas).
+//   bwd_segment_sum_kernel  only then: adds a cut item's segments in order -> bf16.
 //   attn_bwd_dq_kernel    one CTA per SM, persistent over (head, 128-row query block).
 //
 // attn_bwd_dkdv_kernel, 352 threads:
@@ -44,7 +45,7 @@
 //               P phase (P^T = exp2(qk_scale (S^T - lse / qk_scale)), bf16 over the
 //               group's S^T columns), dS phase (dS^T = P^T o (dP^T - Delta), bf16 over the
 //               group's dP^T columns), and per item one of dV / dK -> bf16 global
-//               (fp32 partial sums in the workspace when the items are query parts).
+//               (fp32 partial sums in the workspace for a segment of a cut item).
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
 // Shared memory: K, V (one tile each), Q and dO (2 stages each, 128-byte swizzle), the
 // ones tile and the lse_ext / d_ext rows (128 x 16 bf16, 32-byte swizzle).
@@ -63,6 +64,7 @@ using namespace sm100;
 
 constexpr int kBlk = 128;       // keys per item, queries per block
 constexpr int kThreads = 352;
+constexpr int kPrefetch = 3;    // query blocks between an L2 prefetch and the block's load
 
 template <int D>
 struct BwdTc {
@@ -96,40 +98,79 @@ struct BwdTcParams {
   unsigned int* err;
   int mtiles;   // query blocks per head
   int ktiles;   // key blocks per head
-  int items;    // B * H * ktiles * nsplit
+  int items;    // B * H * ktiles
   int nq_pad;   // mtiles * 128
   int hgroup;   // heads per group of the causal order (causal_head_group)
-  int nsplit;   // query parts per (head, key block) when non-causal (bwd_key_split)
+  int streamk;  // 1: CTA c walks units [work c / G, work (c + 1) / G), G = gridDim.x
+  int work;     // items * mtiles (key block, query block) units (stream-K only)
 };
 
-// One dK/dV item: key block kb of head bh over `count` query blocks starting at q0.
-// Non-causal items walk their range from a rotated start (rot), so that the CTAs of one
-// head do not all read the same query block at once; part is the item's query part
-// (0 unless the items are split, bwd_key_split).
+// One dK/dV item (or segment of one): key block kb of head bh over `count` query blocks
+// starting at q0.  Whole non-causal items walk their range from a rotated start (rot),
+// so that the CTAs of one head do not all read the same query block at once.  slot: -1
+// stores bf16 dV and dK; else the segment's fp32 partial sums go to that workspace slot.
 struct BwdItem {
-  int bh, kb, q0, count, rot, part;
+  int bh, kb, q0, count, rot, slot;
 };
 
+// First unit of CTA c's stream-K range.
+__device__ __forceinline__ int sk_start(int work, int c, int G) {
+  return static_cast<int>(static_cast<long long>(work) * c / G);
+}
+
+// The CTA's items: idx runs from bwd_first to bwd_end in steps of bwd_step.  kSK false,
+// one CTA per item: idx is the item, stepping by gridDim.x.  kSK true (stream-K): idx is
+// the first unit of a segment of the CTA's range, which ends at the next item boundary
+// or the range end.  (The two are separate kernel instances: with the range arithmetic
+// in it, the one-CTA-per-item loop kept its item values out of the uniform registers
+// and ran 5% slower.)
+template <bool kSK>
+__device__ __forceinline__ int bwd_first(const BwdTcParams& p) {
+  if constexpr (kSK) return sk_start(p.work, blockIdx.x, gridDim.x);
+  else return static_cast<int>(blockIdx.x);
+}
+
+template <bool kSK>
+__device__ __forceinline__ int bwd_end(const BwdTcParams& p) {
+  if constexpr (kSK) return sk_start(p.work, blockIdx.x + 1, gridDim.x);
+  else return p.items;
+}
+
+template <bool kSK>
 __device__ __forceinline__ BwdItem bwd_item(int idx, const BwdTcParams& p) {
-  const int BH = p.a.B * p.a.H;
   BwdItem t;
-  if (p.a.causal) {  // longest first (small key blocks see the most queries), heads in groups
-    causal_item(idx, BH, p.ktiles, p.hgroup, t.bh, t.kb);
-    t.q0 = t.kb;
-    t.count = p.mtiles - t.kb;
+  t.slot = -1;
+  if constexpr (!kSK) {
+    if (p.a.causal) {  // longest first (small key blocks see the most queries), heads in groups
+      causal_item(idx, p.a.B * p.a.H, p.ktiles, p.hgroup, t.bh, t.kb);
+      t.q0 = t.kb;
+      t.count = p.mtiles - t.kb;
+      t.rot = 0;
+    } else {           // head-major: the CTAs running together share one head's Q/dO in L2
+      t.bh = idx / p.ktiles;
+      t.kb = idx - t.bh * p.ktiles;
+      t.q0 = 0;
+      t.count = p.mtiles;
+      t.rot = t.kb % t.count;
+    }
+  } else {
+    const int M = p.mtiles;
+    const int item = idx / M;
+    t.bh = item / p.ktiles;
+    t.kb = item - t.bh * p.ktiles;
+    t.q0 = idx - item * M;
+    t.count = min((item + 1) * M, bwd_end<true>(p)) - idx;
     t.rot = 0;
-    t.part = 0;
-  } else {           // head-major: the CTAs running together share one head's Q/dO in L2
-    const int per_head = p.ktiles * p.nsplit;
-    t.bh = idx / per_head;
-    const int rem = idx - t.bh * per_head;
-    t.kb = rem / p.nsplit;
-    t.part = rem - t.kb * p.nsplit;
-    t.q0 = (t.part * p.mtiles) / p.nsplit;
-    t.count = ((t.part + 1) * p.mtiles) / p.nsplit - t.q0;
-    t.rot = t.kb % t.count;
+    if (t.q0 != 0 || t.count != M)
+      t.slot = 2 * static_cast<int>(blockIdx.x) + (idx == bwd_first<true>(p) ? 0 : 1);
   }
   return t;
+}
+
+template <bool kSK>
+__device__ __forceinline__ int bwd_step(int idx, const BwdItem& t) {
+  if constexpr (kSK) return idx + t.count;
+  else return idx + static_cast<int>(gridDim.x);
 }
 
 // query block of the item's ii-th step
@@ -152,7 +193,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Bounds of 384 threads cap registers at 168 per thread: with 11 warps, three share a
 // sub-partition's 16K registers, so a 352-thread CTA cannot launch with more.
-template <int D>
+template <int D, bool kSK>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -222,8 +263,9 @@ __global__ void __launch_bounds__(384, 1)
         ++qc;
         return true;
       };
-      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-        const BwdItem t = bwd_item(idx, p);
+      for (int idx = bwd_first<kSK>(p), end = bwd_end<kSK>(p), nx; idx < end && ok; idx = nx, ++it) {
+        const BwdItem t = bwd_item<kSK>(idx, p);
+        nx = bwd_step<kSK>(idx, t);
         const int bh = t.bh, kb = t.kb, count = t.count;
         ok = mbar_wait(bar(B_KV_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
         if (!ok) break;
@@ -247,6 +289,19 @@ __global__ void __launch_bounds__(384, 1)
                         64 * c, blk * kBlk, bh);
           tma_load_3d(base + C::kOffDX + dst * C::kExtBytes, &tmDX, fb, 0, blk * kBlk, bh);
           ++dc;
+          // Q and dO of the block kPrefetch ahead into L2: when the CTAs running together
+          // stream different heads (stream-K ranges), a block's first read comes from
+          // DRAM, which the two-stage rings alone do not cover.  (With one CTA per item
+          // the CTAs share one head and the prefetches only add L2 traffic: 5% slower.)
+          if (kSK && ii + kPrefetch < count) {
+            const int pb = block_at(t, ii + kPrefetch) * kBlk;
+            for (int c = 0; c < C::kChunks; ++c) {
+              tma_prefetch_l2_3d(&tmQ, 64 * c, pb, bh);
+              tma_prefetch_l2_3d(&tmDO, 64 * c, pb, bh);
+            }
+            tma_prefetch_l2_3d(&tmQX, 0, pb, bh);
+            tma_prefetch_l2_3d(&tmDX, 0, pb, bh);
+          }
           if (ii + 1 < count) ok = load_q(bh, block_at(t, ii + 1));
         }
       }
@@ -286,8 +341,10 @@ __global__ void __launch_bounds__(384, 1)
         issued = true;
       };
       ok = w(bar(B_ONES_FULL), 0);
-      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-        const int count = bwd_item(idx, p).count;
+      for (int idx = bwd_first<kSK>(p), end = bwd_end<kSK>(p), nx; idx < end && ok; idx = nx, ++it) {
+        const BwdItem t = bwd_item<kSK>(idx, p);
+        nx = bwd_step<kSK>(idx, t);
+        const int count = t.count;
         ok = w(bar(B_KV_FULL), it & 1) && wait_q(qc);
         if (ok) issue_s(qc);
         for (int ii = 0; ii < count && ok; ++ii, ++qc) {
@@ -352,8 +409,10 @@ __global__ void __launch_bounds__(384, 1)
         issued = true;
       };
       ok = w(bar(B_ONES_FULL), 0);
-      for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-        const int count = bwd_item(idx, p).count;
+      for (int idx = bwd_first<kSK>(p), end = bwd_end<kSK>(p), nx; idx < end && ok; idx = nx, ++it) {
+        const BwdItem t = bwd_item<kSK>(idx, p);
+        nx = bwd_step<kSK>(idx, t);
+        const int count = t.count;
         ok = w(bar(B_KV_FULL), it & 1) && wait_do(qc);
         if (ok) issue_dp(qc);
         for (int ii = 0; ii < count && ok; ++ii, ++qc) {
@@ -537,8 +596,9 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t qc = 0;
     int it = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
-      const BwdItem t = bwd_item(idx, p);
+    for (int idx = bwd_first<kSK>(p), end = bwd_end<kSK>(p), nx; idx < end && ok; idx = nx, ++it) {
+      const BwdItem t = bwd_item<kSK>(idx, p);
+      nx = bwd_step<kSK>(idx, t);
       const int bh = t.bh, kb = t.kb, count = t.count;
       const int key = kb * kBlk + r;
       const bool key_ok = key < p.a.Nkv;
@@ -561,10 +621,10 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t tcol = h ? C::kTmemDK : C::kTmemDV;
       uint16_t* out = h ? p.a.dk : p.a.dv;
       const float scale = h ? p.a.sm_scale : 1.0f;
-      // a query part stores its fp32 partial sums (dK unscaled); bwd_part_sum_kernel
-      // adds the parts in order and converts
-      float* part = p.nsplit > 1
-                        ? p.a.part + (static_cast<size_t>(t.part) * 2 + h) * p.a.B * p.a.H * p.a.Nkv * D + grow
+      // a segment of a cut item stores its fp32 partial sums (dK unscaled) in its slot;
+      // bwd_segment_sum_kernel adds an item's segments in order and converts
+      float* part = kSK && t.slot >= 0
+                        ? p.a.part + ((static_cast<size_t>(t.slot) * 2 + h) * kBlk + r) * D
                         : nullptr;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -675,26 +735,47 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
   }
 }
 
-// Adds the query parts' partial sums of dV and dK in part order and stores them as bf16
-// (dK times sm_scale): n4 float4s per tensor, parts laid out [part][dV, dK][n4].
-__global__ void __launch_bounds__(256) bwd_part_sum_kernel(const float4* __restrict__ part,
-                                                           int nsplit, long long n4,
-                                                           float sm_scale, uint2* dv, uint2* dk) {
+// Stream-K fix-up: for every item that range boundaries cut, adds its segments' fp32
+// partial sums in CTA order (the CTAs c0..c1 whose ranges meet the item; a segment sits
+// in slot 2c when it is CTA c's first, else 2c + 1) and stores bf16 dV and dK (x
+// sm_scale).  One thread per 4 columns of one key row of dV or dK.  Items inside one
+// range were stored by the dK/dV kernel directly.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_segment_sum_kernel(const float4* __restrict__ part,
+                                                              int work, int G, int mtiles,
+                                                              int ktiles, long long items,
+                                                              int Nkv, float sm_scale,
+                                                              uint2* dv, uint2* dk) {
+  constexpr int kD4 = D / 4;
+  const long long per_item = 2ll * kBlk * kD4;
   const long long stride = static_cast<long long>(gridDim.x) * 256;
-  for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < 2 * n4;
+  for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < items * per_item;
        i += stride) {
-    const int t = i >= n4 ? 1 : 0;
-    const long long j = i - t * n4;
-    float4 acc = part[t * n4 + j];
-    for (int s = 1; s < nsplit; ++s) {
-      const float4 x = part[(2ll * s + t) * n4 + j];
+    const long long item = i / per_item;
+    const int rem = static_cast<int>(i - item * per_item);
+    const int t = rem / (kBlk * kD4);                    // 0: dV, 1: dK
+    const int row = (rem / kD4) % kBlk;
+    const int c4 = rem % kD4;
+    const int kb = static_cast<int>(item % ktiles);
+    if (kb * kBlk + row >= Nkv) continue;
+    const long long first = item * mtiles, last = first + mtiles - 1;
+    // CTA whose range holds unit u: the last c with work c / G <= u
+    const int c0 = static_cast<int>(((first + 1) * G - 1) / work);
+    const int c1 = static_cast<int>(((last + 1) * G - 1) / work);  // (64-bit products)
+    if (c0 == c1) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c0; c <= c1; ++c) {
+      const long long slot = 2ll * c + (sk_start(work, c, G) >= first ? 0 : 1);
+      const float4 x = part[((slot * 2 + t) * kBlk + row) * kD4 + c4];
       acc.x += x.x;
       acc.y += x.y;
       acc.z += x.z;
       acc.w += x.w;
     }
     const float sc = t ? sm_scale : 1.0f;
-    (t ? dk : dv)[j] = make_uint2(pack_bf16x2(acc.x * sc, acc.y * sc), pack_bf16x2(acc.z * sc, acc.w * sc));
+    const long long bh = item / ktiles;
+    const long long o = ((bh * Nkv) + kb * kBlk + row) * kD4 + c4;
+    (t ? dk : dv)[o] = make_uint2(pack_bf16x2(acc.x * sc, acc.y * sc), pack_bf16x2(acc.z * sc, acc.w * sc));
   }
 }
 
@@ -707,8 +788,14 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   p.err = err;
   p.mtiles = (a.Nq + kBlk - 1) / kBlk;
   p.ktiles = (a.Nkv + kBlk - 1) / kBlk;
-  p.nsplit = a.causal || a.part == nullptr ? 1 : a.nsplit;
-  p.items = BH * p.ktiles * p.nsplit;
+  p.items = BH * p.ktiles;
+  // stream-K: at most the CTAs the workspace has slots for, each with >= 4 units
+  const long long work = static_cast<long long>(p.items) * p.mtiles;
+  int G = a.causal || a.part == nullptr ? 0 : a.sk_ctas;
+  if (G > num_sms) G = num_sms;
+  if (G > 0 && (work < 4ll * G || work > (1ll << 30))) G = 0;
+  p.work = G > 0 ? static_cast<int>(work) : 0;
+  p.streamk = G > 0;
   p.nq_pad = p.mtiles * kBlk;
   // a causal item streams its head's Q and dO blocks
   p.hgroup = causal_head_group(4ll * a.Nq * D, BH);
@@ -727,20 +814,21 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
       !make_ext_map_3d(&mqx, a.lse_ext, p.nq_pad, BH) ||
       !make_ext_map_3d(&mdx, a.d_ext, p.nq_pad, BH) || !make_ext_map_3d(&mones, a.ones, 128, 1))
     return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = p.streamk ? attn_bwd_dkdv_kernel<D, true> : attn_bwd_dkdv_kernel<D, false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int grid = p.items < num_sms ? p.items : num_sms;
-  attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, mqx, mdx, mones, p);
+  const int grid = p.streamk ? G : (p.items < num_sms ? p.items : num_sms);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mdo, mqx, mdx, mones, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (p.nsplit > 1) {
-    const long long n4 = static_cast<long long>(BH) * a.Nkv * D / 4;
-    long long blocks = (2 * n4 + 255) / 256;
+  if (p.streamk) {
+    const long long n = static_cast<long long>(p.items) * 2 * kBlk * (D / 4);
+    long long blocks = (n + 255) / 256;
     if (blocks > static_cast<long long>(num_sms) * 16) blocks = static_cast<long long>(num_sms) * 16;
-    bwd_part_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(a.part), p.nsplit, n4, a.sm_scale,
-        reinterpret_cast<uint2*>(a.dv), reinterpret_cast<uint2*>(a.dk));
+    bwd_segment_sum_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(a.part), p.work, G, p.mtiles, p.ktiles, p.items, a.Nkv,
+        a.sm_scale, reinterpret_cast<uint2*>(a.dv), reinterpret_cast<uint2*>(a.dk));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

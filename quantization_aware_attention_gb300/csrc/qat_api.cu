@@ -188,7 +188,7 @@ qat_status_t qat_attn_merge(float* o_q_acc, float* o_hp_acc, float* lse_acc,
 size_t qat_attn_bwd_workspace_bytes(int B, int H, int Nq, int Nkv, int D) {
   bool empty = false;
   if (check_sizes(B, H, Nq, Nkv, D, 1.0f, 0, 0, &empty) != QAT_OK) return 0;
-  return qat::bwd_workspace_layout(B, H, Nq, Nkv, D, qat::bwd_key_split(B, H, Nq, Nkv)).total;
+  return qat::bwd_workspace_layout(B, H, Nq, Nkv, D, qat::bwd_stream_k_ctas(B, H, Nq, Nkv)).total;
 }
 
 }  // extern "C"
@@ -216,17 +216,16 @@ qat_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o
   const void* ptrs[] = {q, k, v, o_hp, lse, dO, dq, dk, dv};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return QAT_ERR_INVALID_ARG;
-  // the query-part split of the dK/dV items runs only when the workspace also holds its
-  // partial sums (qat_attn_bwd_workspace_bytes does; the no-alloc scratch may not)
-  const size_t need = qat::bwd_workspace_layout(B, H, Nq, Nkv, D, 1).total;
+  // the stream-K split of the dK/dV work runs only when the workspace also holds its
+  // segment sums (qat_attn_bwd_workspace_bytes does; the no-alloc scratch may not)
+  const size_t need = qat::bwd_workspace_layout(B, H, Nq, Nkv, D, 0).total;
   if (workspace == nullptr || workspace_bytes < need) return QAT_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return QAT_ERR_INVALID_ARG;
-  int nsplit = causal ? 1 : qat::bwd_key_split(B, H, Nq, Nkv);
-  if (nsplit > 1 && workspace_bytes < qat::bwd_workspace_layout(B, H, Nq, Nkv, D, nsplit).total)
-    nsplit = 1;
+  int sk = causal ? 0 : qat::bwd_stream_k_ctas(B, H, Nq, Nkv);
+  if (sk > 0 && workspace_bytes < qat::bwd_workspace_layout(B, H, Nq, Nkv, D, sk).total) sk = 0;
 
   qat::BwdArgs a;
-  const qat::BwdWorkspace wl = qat::bwd_workspace_layout(B, H, Nq, Nkv, D, nsplit);
+  const qat::BwdWorkspace wl = qat::bwd_workspace_layout(B, H, Nq, Nkv, D, sk);
   char* ws = static_cast<char*>(workspace);
   a.q = static_cast<const uint16_t*>(q);
   a.k = static_cast<const uint16_t*>(k);
@@ -242,9 +241,9 @@ qat_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o
   a.lse_ext = reinterpret_cast<uint16_t*>(ws + wl.off_lse_ext);
   a.d_ext = reinterpret_cast<uint16_t*>(ws + wl.off_d_ext);
   a.ones = reinterpret_cast<uint16_t*>(ws + wl.off_ones);
-  a.part = nsplit > 1 ? reinterpret_cast<float*>(ws + wl.off_part) : nullptr;
+  a.part = sk > 0 ? reinterpret_cast<float*>(ws + wl.off_part) : nullptr;
   a.k_mean = k_mean;
-  a.nsplit = nsplit;
+  a.sk_ctas = sk;
   a.B = B; a.H = H; a.Nq = Nq; a.Nkv = Nkv; a.D = D;
   a.sm_scale = sm_scale;
   a.qk_scale = sm_scale * kLog2e;

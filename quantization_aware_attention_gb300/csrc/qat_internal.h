@@ -49,14 +49,14 @@ inline qat_status_t check_sizes(int B, int H, int Nq, int Nkv, int D, float sm_s
 //   ones             bf16 [128, 16]: 1 in elements 0-2 of every row
 // The dK/dV kernel multiplies ones by lse_ext (d_ext) in one extra MMA k-step, so its
 // score accumulators come out as S^T - lse / qk_scale and dP^T - Delta.
-// With the query blocks of each dK/dV item split into nsplit > 1 parts (bwd_key_split),
-// the layout ends with the parts' partial sums:
-//   part             fp32 [nsplit][2][B, H, Nkv, D], [s][0] = dV and [s][1] = dK / sm_scale
+// With the non-causal dK/dV work cut into ranges (bwd_stream_k_ctas returns G > 0), the
+// layout ends with the segments' partial sums, two slots per CTA:
+//   part             fp32 [2G][2][128][D], [slot][0] = dV and [slot][1] = dK / sm_scale
 struct BwdWorkspace {
   size_t nq_pad, off_lse, off_delta, off_lse_ext, off_d_ext, off_ones, off_part, total;
 };
 
-inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int Nkv, int D, int nsplit) {
+inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int Nkv, int D, int sk_ctas) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   BwdWorkspace w;
   w.nq_pad = (static_cast<size_t>(Nq) + 127) / 128 * 128;
@@ -67,40 +67,39 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int Nkv, int D, i
   w.off_d_ext = w.off_lse_ext + up(rows_pad * 32);
   w.off_ones = w.off_d_ext + up(rows_pad * 32);
   w.off_part = w.off_ones + up(128 * 32);
-  const size_t part = nsplit > 1 ? static_cast<size_t>(nsplit) * 2 * B * H * Nkv * D * sizeof(float) : 0;
+  const size_t part = sk_ctas > 0 ? static_cast<size_t>(sk_ctas) * 2 * 2 * 128 * D * sizeof(float) : 0;
   w.total = w.off_part + up(part);
   if (w.total == 0) w.total = 256;
   return w;
 }
 
-// Query parts per non-causal dK/dV item (one head x one 128-key block).  The grid has
-// one CTA per SM, so with few items the last wave runs ragged: B1 H40 Nkv512 has 160
-// items of 128 query blocks each, and 8 CTAs ran two while the rest idled half the
-// time.  Splitting every item's query blocks into nsplit parts gives nsplit times the
-// items; each part keeps fp32 partial sums that one more kernel adds in part order,
-// so the result stays deterministic.  The choice minimises an estimated makespan,
-// waves x (blocks per part + about two blocks of per-item cost), for 152 SMs: it
-// depends on the sizes only, so the workspace size does too.  A split must clearly
-// beat the alternative (5%), and every part keeps at least 4 query blocks.
-inline int bwd_key_split(int B, int H, int Nq, int Nkv) {
-  constexpr long long kSms = 152;
-  constexpr int kMinBlocks = 4, kMaxSplit = 32;
+// Work split of the non-causal dK/dV kernel.  One CTA runs per SM, so with few (head,
+// 128-key block) items the last wave runs ragged: B1 H40 Nkv512 has 160 items of 128
+// query blocks each, and 8 CTAs ran two while the rest idled half the time.  Then the
+// kernel runs stream-K: the items' (key block, query block) units, in head-major item
+// order, are cut into G equal contiguous ranges, one per CTA.  A CTA walks its range
+// item by item; an item cut by a range boundary is done in segments, each of which
+// stores fp32 partial sums of dV and dK (the CTA's first segment in slot 2c, its last in
+// 2c + 1), and one more kernel adds an item's segments in CTA order, so the result stays
+// deterministic.  Each range has at least 4 units.  The choice compares estimated
+// makespans, ~2 blocks of fixed cost per item or segment, for 152 SMs, from the sizes
+// alone, so the workspace size is a function of the sizes too.  With many items the
+// ragged wave costs little and the head-major item order, which keeps the CTAs running
+// together on one head's Q and dO in L2, is kept: returns 0.
+inline int bwd_stream_k_ctas(int B, int H, int Nq, int Nkv) {
+  constexpr long long kSms = 152, kMinSeg = 4;
   const long long items = static_cast<long long>(B) * H * ((Nkv + 127) / 128);
-  const int M = (Nq + 127) / 128;
-  if (items <= 0 || M < 2 * kMinBlocks) return 1;
-  auto cost = [&](int ns) {
-    return ((items * ns + kSms - 1) / kSms) * ((M + ns - 1) / ns + 2);
-  };
-  int best = 1;
-  long long best_cost = cost(1);
-  for (int ns = 2; ns <= kMaxSplit && ns * kMinBlocks <= M; ++ns) {
-    const long long c = cost(ns);
-    if (c * 100 < best_cost * 95) {
-      best = ns;
-      best_cost = c;
-    }
-  }
-  return best;
+  const long long M = (Nq + 127) / 128;
+  if (items <= 0 || M < 2) return 0;
+  const long long W = items * M;
+  if (W > (1ll << 30)) return 0;  // the kernel's range arithmetic is 32-bit
+  long long G = W / kMinSeg;
+  if (G > kSms) G = kSms;
+  if (G < 1) return 0;
+  const double classic = static_cast<double>((items + kSms - 1) / kSms) * (M + 2);
+  const double per_cta = static_cast<double>(W) / G;
+  const double split = per_cta + 2.0 * (per_cta / M + 2.0);
+  return split < 0.95 * classic ? static_cast<int>(G) : 0;
 }
 
 // [BH, N, D] bf16 viewed as a 3-D TMA tensor (D innermost), 64 x 128 x 1 boxes,
@@ -144,9 +143,9 @@ struct BwdArgs {
   uint16_t* lse_ext;  // bf16 [B, H, Nq_pad, 16] (see BwdWorkspace)
   uint16_t* d_ext;    // bf16 [B, H, Nq_pad, 16]
   uint16_t* ones;     // bf16 [128, 16]
-  float* part;        // dK/dV partial sums (BwdWorkspace::off_part) when nsplit > 1
+  float* part;        // dK/dV segment sums (BwdWorkspace::off_part) when sk_ctas > 0
   const float* k_mean;  // fp32 [D] or null: smooth_k's channel mean (dQ's SMOOTH_K term)
-  int nsplit;         // query parts per dK/dV item: 1, or bwd_key_split(...) (non-causal)
+  int sk_ctas;        // 0, or the stream-K CTA bound of bwd_stream_k_ctas (non-causal)
   int B, H, Nq, Nkv, D;
   float sm_scale;
   float qk_scale;

@@ -59,9 +59,9 @@ extern "C" qat_status_t qat_attn_bwd_noalloc(const void* q, const void* k, const
   const void* ptrs[] = {q, k, v, o_hp, lse, dO, dq, dk, dv};
   for (const void* p : ptrs)
     if (p == nullptr || !qat::aligned16(p)) return QAT_ERR_INVALID_ARG;
-  // the scratch must hold the workspace without the dK/dV query-part sums; qat_attn_bwd
-  // uses the split only when those fit as well
-  if (qat::bwd_workspace_layout(B, H, Nq, Nkv, D, 1).total > kNoAllocScratchBytes)
+  // the scratch must hold the workspace without the dK/dV segment sums; qat_attn_bwd
+  // uses the stream-K split only when those fit as well
+  if (qat::bwd_workspace_layout(B, H, Nq, Nkv, D, 0).total > kNoAllocScratchBytes)
     return QAT_ERR_WORKSPACE;
   void* scratch = nullptr;
   const qat_status_t sst = scratch_on_current_device(&scratch);

@@ -138,6 +138,15 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
 }
 
 // 3-D tiled load of one box into shared memory, completing `bytes` on `bar`.
+// Prefetches one tile of a 3-D tensor map into L2 (no shared memory, no barrier): the
+// x coordinate follows the same 16-byte rule as a load.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                             int c0, int c1, int c2) {
   asm volatile(

@@ -96,21 +96,25 @@ def test_backward_validation(kw, want):
 
 
 def _base_workspace(B, H, Nq):
-    """The workspace without dK/dV query parts: lse and Delta (fp32), the two 16-element
+    """The workspace without dK/dV segment sums: lse and Delta (fp32), the two 16-element
     bf16 extension rows per padded query row, and the 128 x 16 bf16 ones tile."""
     up = lambda x: (x + 255) // 256 * 256
     rows = B * H * ((Nq + 127) // 128 * 128)
     return 2 * up(rows * 4) + 2 * up(rows * 32) + up(128 * 32)
 
 
-def test_workspace_holds_query_part_sums_only_for_few_key_items():
-    # c4: 10240 (head, key block) items, no split
+def test_workspace_holds_segment_sums_only_for_few_key_items():
+    # c4: 10240 (head, key block) items, 67 per SM: one CTA per item, no partial sums
     assert capi.qat_attn_bwd_workspace_bytes(1, 40, 32768, 32768, 128) == _base_workspace(1, 40, 32768)
-    # c5b: 160 items of 128 query blocks on a 152-SM grid -> 4 query parts of fp32 dV, dK
+    # c5b: 160 items of 128 query blocks on 152 SMs -> stream-K over 152 CTAs, two
+    # 128-row slots of fp32 dV and dK per CTA
     extra = capi.qat_attn_bwd_workspace_bytes(1, 40, 16384, 512, 128) - _base_workspace(1, 40, 16384)
-    assert extra == 4 * 2 * 40 * 512 * 128 * 4
-    # fewer than 8 query blocks: never split
+    assert extra == 152 * 2 * 2 * 128 * 128 * 4
+    # one item of 7 query blocks: two CTAs would not pay for their partial sums
     assert capi.qat_attn_bwd_workspace_bytes(1, 1, 896, 100, 64) == _base_workspace(1, 1, 896)
+    # 2 items x 16 query blocks: 8 CTAs of 4 blocks (at least 4 per range)
+    extra = capi.qat_attn_bwd_workspace_bytes(1, 1, 2000, 130, 64) - _base_workspace(1, 1, 2000)
+    assert extra == 8 * 2 * 2 * 128 * 64 * 4
 
 
 def test_workspace_bytes():

@@ -119,8 +119,8 @@ def test_c5b_cross_attention_sampled_heads():
     (2, 1, 100, 37, 64, False),
     (1, 1, 200, 200, 128, True),
     (1, 1, 7, 300, 128, False),
-    (1, 2, 1100, 300, 128, False),  # few (head, key block) items: query blocks in 2 parts
-    (1, 1, 2000, 130, 64, False),   # 4 parts, D = 64
+    (1, 2, 1100, 300, 128, False),  # few (head, key block) items: stream-K ranges
+    (1, 1, 2000, 130, 64, False),   # stream-K, items in 4 segments, D = 64
 ])
 def test_edge_shapes(B, H, Nq, Nkv, D, causal):
     inp = custom_inputs(500 + Nq + Nkv, B, H, Nq, Nkv, D)
@@ -158,9 +158,9 @@ def test_deterministic(causal):
 
 
 def test_deterministic_with_query_parts():
-    """With few (head, key block) items the dK/dV kernel splits each item's query blocks
-    into parts and a second kernel adds the parts' fp32 sums in a fixed order, so dK and
-    dV stay bit-identical run to run."""
+    """With few (head, key block) items the dK/dV kernel runs stream-K: equal ranges of
+    the items' query blocks per CTA, cut items storing fp32 partial sums that a second
+    kernel adds in CTA order, so dK and dV stay bit-identical run to run."""
     inp = custom_inputs(93, 1, 1, 2000, 130, 64)
     a = run_gpu(inp, False, 0.125)
     b = run_gpu(inp, False, 0.125)
@@ -168,16 +168,44 @@ def test_deterministic_with_query_parts():
         assert torch.equal(a[n], b[n]), n
 
 
+def _at_16_byte_offset(t):
+    """A copy of t whose storage starts 16 bytes past a 256-byte boundary: aligned as the
+    C ABI requires (16 bytes) but not to 32 bytes."""
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    view = buf[8:].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 32 == 16
+    return view
+
+
+def test_inputs_16_byte_aligned_match_aligned():
+    """Q (and the other inputs) at 16-byte but not 32-byte aligned addresses give bit-
+    identical outputs: the dQ kernel's 32-byte row loads are used only on 32-byte aligned
+    q, and every other access needs 16 bytes."""
+    inp = custom_inputs(95, 1, 2, 300, 700, 128)
+    a = run_gpu(inp, False, 0.088)
+    q, k, v, do = (_at_16_byte_offset(dev_bf16(inp[n])) for n in ("q", "k", "v", "do"))
+    o_q, o_hp, lse = qat_attention_forward(q, k, v, False, 0.088)
+    dq, dk, dv = qat_attention_backward(q, k, v, o_hp, lse, do, False, 0.088)
+    torch.cuda.synchronize()
+    assert capi.qat_attn_device_status() == Status.OK
+    for n, t in (("o_q", o_q), ("o_hp", o_hp), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.equal(a[n], t), n
+
+
 def test_query_part_split_without_room_for_its_sums_runs_unsplit():
-    """A workspace that holds everything but the dK/dV parts' partial sums (as the no-alloc
-    scratch may) runs the backward without the split: the same gradients up to the fp32
-    summation order.  One byte less than that is refused."""
+    """A workspace that holds everything but the dK/dV segments' partial sums (as the
+    no-alloc scratch may) runs the backward with one CTA per item instead of stream-K:
+    the same gradients up to the fp32 summation order.  One byte less than that is
+    refused."""
     B, H, Nq, Nkv, D, sc = 1, 1, 2000, 130, 64, 0.125
     inp = custom_inputs(94, B, H, Nq, Nkv, D)
     q, k, v, do = (dev_bf16(inp[n]) for n in ("q", "k", "v", "do"))
     _, o_hp, lse = qat_attention_forward(q, k, v, False, sc)
     full = capi.qat_attn_bwd_workspace_bytes(B, H, Nq, Nkv, D)
-    base = full - 4 * 2 * B * H * Nkv * D * 4  # 4 query parts of fp32 dV and dK
+    # 2 items x 16 query blocks: 8 stream-K CTAs of 4 blocks, two 128-row slots of fp32
+    # dV and dK each
+    base = full - 8 * 2 * 2 * 128 * D * 4
     outs = {}
     for name, nbytes in (("split", full), ("unsplit", base)):
         ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")

@@ -39,7 +39,7 @@ def _rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-# (B, H, Nq, Nkv, D), causal, seed; the third splits its dK/dV items into query parts,
+# (B, H, Nq, Nkv, D), causal, seed; the third runs its dK/dV work stream-K (cut items,
 # whose fp32 partial sums also live in the scratch
 PROBLEMS = {"A": ((1, 3, 200, 200, 128), True, 11), "B": ((2, 2, 77, 150, 64), False, 12),
             "C": ((1, 1, 2000, 130, 64), False, 13)}
@@ -62,7 +62,7 @@ def _run(name):
 
 
 def test_noalloc_matches_workspace_entry_on_calls_in_a_row():
-    """Same kernels, same query-part split, deterministic sums: the no-alloc gradients
+    """Same kernels, same stream-K split, deterministic sums: the no-alloc gradients
     equal the workspace entry's bit for bit, call after call; A's second run equals its
     first, and A agrees with the oracle within the parity tolerance."""
     first = None
