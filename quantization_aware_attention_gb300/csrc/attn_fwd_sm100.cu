@@ -125,7 +125,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Bounds of 384 threads cap registers at 168 per thread: with 11 warps, three share a
 // sub-partition's 16K registers, so a 352-thread CTA cannot launch with more.
-template <int D>
+// kDefer: each item's epilogue waits for the next item's first block of P (short items,
+// see the softmax warps); a separate instance, since with the epilogue inside the block
+// loop long items ran 2-4% slower.
+template <int D, bool kDefer>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -195,6 +198,13 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(base + C::kOffQ + c * C::kChunkBytes, &tmQ, bar(BAR_Q_FULL), 64 * c,
                       mt * kBM, bh);
+        // the next item's Q tile into L2 (each Q tile is read once, so from DRAM): its
+        // load then waits only for the L2 when the Q buffer frees up
+        if (idx + static_cast<int>(gridDim.x) < p.items) {
+          int nbh, nmt;
+          item_coords(idx + gridDim.x, p, nbh, nmt);
+          for (int c = 0; c < C::kChunks; ++c) tma_prefetch_l2_3d(&tmQ, 64 * c, nmt * kBM, nbh);
+        }
         for (int j = 0; j <= J && ok; ++j) {
           if (j < J) {  // K_j
             const uint32_t st = kc % kKStages, use = kc / kKStages;
@@ -359,6 +369,67 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       return w;
     };
+    // With kDefer an item's epilogue runs after the next item's first block of P, so that
+    // the wait for its last PV products and the next item's first score product overlap
+    // the softmax of that block instead of following the epilogue (at B1 H40 Nq16384
+    // Nkv512, 4 blocks per item: 0.272 -> 0.252 ms).  O stays in TMEM until then: the
+    // next item's first PV waits for O_EMPTY, and a rescale needs j > 0.
+    int e_bh = 0, e_mt = 0, e_it = -1;  // the item whose epilogue is pending (e_it >= 0)
+    float e_m = 0.f, e_l = 1.f;         // its running max and row sum
+    auto epilogue = [&]() -> bool {
+      // O_DONE cannot be used here: it completes once per block, and at the end of an
+      // item the PV products of the last two blocks may both still be running (S of
+      // the last block only waited for PV two blocks back).  A parity wait on a barrier
+      // two phases behind passes at once, so the epilogue waits on O_FINAL, committed
+      // after the item's last PV: one phase per item.
+      if (!wwait(bar(BAR_O_FINAL), e_it & 1)) return false;
+      tc_fence_after();
+      const float inv_l = 1.0f / e_l;
+      const int row = e_mt * kBM + r;
+      const bool in = row < p.a.Nq;
+      // the warp's first row, and how many of its 32 rows exist
+      const int wrow = e_mt * kBM + 32 * quarter;
+      const int wvalid = min(32, p.a.Nq - wrow);
+      const size_t orow0 = static_cast<size_t>(e_bh) * p.a.Nq + wrow;
+      const uint32_t tO = tbase + lrow + (h ? C::kTmemOhp : C::kTmemOq);
+      uint16_t* out = h ? p.a.o_hp : p.a.o_q;
+      float* out32 = h ? p.a.o_hp_f32 : p.a.o_q_f32;  // partial results stay fp32
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        if (out32 != nullptr) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t* x = o + 16 * half + 4 * i;
+              v[i] = make_uint4(__float_as_uint(__uint_as_float(x[0]) * inv_l),
+                                __float_as_uint(__uint_as_float(x[1]) * inv_l),
+                                __float_as_uint(__uint_as_float(x[2]) * inv_l),
+                                __float_as_uint(__uint_as_float(x[3]) * inv_l));
+            }
+            store_rows64(v, reinterpret_cast<char*>(out32 + orow0 * D + 32 * c + 16 * half),
+                         D * sizeof(float), wvalid);
+          }
+          continue;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        const uint4 v[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
+                            make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
+        store_rows64(v, reinterpret_cast<char*>(out + orow0 * D + 32 * c), D * sizeof(uint16_t), wvalid);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(BAR_O_EMPTY));
+      if (in && h == 0) p.a.lse[static_cast<size_t>(e_bh) * p.a.Nq + row] = e_m + log2f(e_l);
+      e_it = -1;
+      return true;
+    };
     uint32_t sc = 0, pvc = 0;                     // S tiles consumed, PV groups done
     int it = 0;
     bool ok = true;
@@ -454,64 +525,23 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(bar(BAR_P_FULL + b));
         ++sc;
         ++pvc;  // PV_j will be issued once every row has arrived
+        if (kDefer && j == 0 && e_it >= 0 && !(ok = epilogue())) break;  // the previous item's
       }
       if (!ok) break;
-      // ---------------------------------------------------------- epilogue
+      // ---------------------------------------------------------- end of item
+      // the row sum over both groups; the epilogue now, or (kDefer) after the next
+      // item's first P
       xsum[h * 128 + r] = l;
       if (!(ok = exchange())) break;
-      const float l_row = xsum[r] + xsum[128 + r];
-      // O_DONE cannot be used here: it completes once per block, and at the end of an
-      // item the PV products of the last two blocks may both still be running (S of
-      // the last block only waited for PV two blocks back).  A parity wait on a barrier
-      // two phases behind passes at once, so the epilogue waits on O_FINAL, committed
-      // after the item's last PV: one phase per item.
-      ok = wwait(bar(BAR_O_FINAL), it & 1);
-      if (!ok) break;
-      tc_fence_after();
-      const float inv_l = 1.0f / l_row;
-      const bool in = row < p.a.Nq;
-      // the warp's first row, and how many of its 32 rows exist
-      const int wrow = mt * kBM + 32 * quarter;
-      const int wvalid = min(32, p.a.Nq - wrow);
-      const size_t orow0 = static_cast<size_t>(bh) * p.a.Nq + wrow;
-      const uint32_t tO = tbase + lrow + (h ? C::kTmemOhp : C::kTmemOq);
-      uint16_t* out = h ? p.a.o_hp : p.a.o_q;
-      float* out32 = h ? p.a.o_hp_f32 : p.a.o_q_f32;  // partial results stay fp32
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * c, o);
-        tmem_wait_ld();
-        if (out32 != nullptr) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint4 v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t* x = o + 16 * half + 4 * i;
-              v[i] = make_uint4(__float_as_uint(__uint_as_float(x[0]) * inv_l),
-                                __float_as_uint(__uint_as_float(x[1]) * inv_l),
-                                __float_as_uint(__uint_as_float(x[2]) * inv_l),
-                                __float_as_uint(__uint_as_float(x[3]) * inv_l));
-            }
-            store_rows64(v, reinterpret_cast<char*>(out32 + orow0 * D + 32 * c + 16 * half),
-                         D * sizeof(float), wvalid);
-          }
-          continue;
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        const uint4 v[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
-                            make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
-        store_rows64(v, reinterpret_cast<char*>(out + orow0 * D + 32 * c), D * sizeof(uint16_t), wvalid);
-      }
-      // (xsum is rewritten only after the next item's first exchange, which both
-      // groups reach after this read)
-      tc_fence_before();
-      mbar_arrive(bar(BAR_O_EMPTY));
-      if (in && h == 0) p.a.lse[static_cast<size_t>(bh) * p.a.Nq + row] = m_used + log2f(l_row);
+      e_l = xsum[r] + xsum[128 + r];
+      e_m = m_used;
+      e_bh = bh;
+      e_mt = mt;
+      e_it = it;
+      if (!kDefer && !(ok = epilogue())) break;
+    }
+    if constexpr (kDefer) {
+      if (ok && e_it >= 0) ok = epilogue();
     }
   }
   tc_fence_before();
@@ -538,12 +568,14 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a, unsigned int* err, int num_sms, cu
   p.items = BH * p.mtiles;
   // a causal item streams its head's K and V blocks
   p.hgroup = causal_head_group(4ll * a.Nkv * D, BH);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // deferred epilogues for items of at most 8 key blocks (non-causal)
+  const bool defer = !a.causal && a.Nkv <= 8 * kBN;
+  auto kern = defer ? attn_fwd_tc_kernel<D, true> : attn_fwd_tc_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = p.items < num_sms ? p.items : num_sms;
-  attn_fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

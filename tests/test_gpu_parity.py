@@ -256,6 +256,33 @@ def test_forward_deterministic_causal_many_items():
             assert torch.equal(a_, b_)
 
 
+def test_forward_deterministic_short_kv_many_items():
+    """Cross-attention with 4 key blocks per item (the c5b shape, 34 items per CTA): the
+    forward instance that stores an item's outputs after the next item's first block of
+    P.  Every output must be bit-identical across runs, and every row finite (each
+    CTA's last item is stored after its loop)."""
+    B, H, Nq, Nkv, D = 1, 40, 16384, 512, 128
+    gen = torch.Generator(device="cuda").manual_seed(6)
+    q = torch.randn(B, H, Nq, D, device="cuda", generator=gen).to(torch.bfloat16)
+    k, v = (torch.randn(B, H, Nkv, D, device="cuda", generator=gen).to(torch.bfloat16)
+            for _ in range(2))
+    outs = []
+    for _ in range(3):
+        o_q = torch.full_like(q, float("nan"))
+        o_hp = torch.full_like(q, float("nan"))
+        lse = torch.full((B, H, Nq), float("nan"), device="cuda")
+        st = capi.qat_attn_fwd(q, k, v, o_q, o_hp, lse, B, H, Nq, Nkv, D, 1.0 / np.sqrt(D), 0, 1)
+        assert st == Status.OK
+        torch.cuda.synchronize()
+        outs.append((o_q, o_hp, lse))
+    assert capi.qat_attn_device_status() == Status.OK
+    for t in outs[0]:
+        assert torch.isfinite(t).all()
+    for o in outs[1:]:
+        for a_, b_ in zip(outs[0], o):
+            assert torch.equal(a_, b_)
+
+
 def test_backward_deterministic_causal_many_items():
     """The c5a shape, causal, through the backward: dQ, dK and dV bit-identical across
     runs (each CTA sums its own rows in a fixed order; no atomics)."""
