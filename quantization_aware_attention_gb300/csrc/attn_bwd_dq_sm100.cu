@@ -175,13 +175,26 @@ __global__ void __launch_bounds__(384, 1)
       for (int idx = blockIdx.x; idx < p.items && ok; idx += gridDim.x, ++it) {
         int bh, mt, J;
         dq_item(idx, p, bh, mt, J);
-        ok = mbar_wait(bar(Q_DO_EMPTY), (it & 1) ^ 1, abort_flag, p.err);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(Q_DO_FULL), C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(base + C::kOffDO + c * C::kChunkBytes, &tmDO, bar(Q_DO_FULL), 64 * c,
-                      mt * kBlk, bh);
+        // the item's dO waits for the previous item's last dP; its first K and V tiles
+        // only for ring stages, so they go first and the item's first S can follow the
+        // previous item's last one without waiting for that dP
+        auto load_do = [&]() -> bool {
+          if (!mbar_wait(bar(Q_DO_EMPTY), (it & 1) ^ 1, abort_flag, p.err)) return false;
+          mbar_arrive_expect_tx(bar(Q_DO_FULL), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(base + C::kOffDO + c * C::kChunkBytes, &tmDO, bar(Q_DO_FULL), 64 * c,
+                        mt * kBlk, bh);
+          // the next item's dO tile into L2 (each dO tile is read once, so from DRAM)
+          if (idx + static_cast<int>(gridDim.x) < p.items) {
+            int nbh, nmt, nJ;
+            dq_item(idx + gridDim.x, p, nbh, nmt, nJ);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_prefetch_l2_3d(&tmDO, 64 * c, nmt * kBlk, nbh);
+          }
+          return true;
+        };
         for (int j = 0; j < J && ok; ++j) {
+          if (j == 1 && !(ok = load_do())) break;
           {
             const uint32_t st = kc % kKStages, use = kc / kKStages;
             ok = mbar_wait(bar(Q_K_EMPTY + st), (use & 1) ^ 1, abort_flag, p.err);
@@ -203,6 +216,7 @@ __global__ void __launch_bounds__(384, 1)
             ++vc;
           }
         }
+        if (ok && J == 1) ok = load_do();
       }
       // drain: every issued load lands before the CTA exits
       if (it > 0) mbar_wait_drain(bar(Q_DO_FULL), (it - 1) & 1, p.err);
