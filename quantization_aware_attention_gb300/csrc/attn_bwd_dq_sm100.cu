@@ -15,8 +15,9 @@
 // memory, and the epilogue adds rowsum x k_mean before scaling.
 //
 // CTA layout (352 threads, one CTA per SM, persistent over (head, 128-row query block)):
-//   warp 0      TMA producer: the item's dO tile, then K_j (4-stage ring) and V_j
-//               (2-stage ring), 128 rows x D in 128-byte-swizzled boxes.
+//   warp 0      TMA producer: per item K_0 and V_0, the item's dO tile (once the
+//               previous item's last dP has read the buffer), then the other K_j (4-stage
+//               ring) and V_j (2-stage ring), 128 rows x D in 128-byte-swizzled boxes.
 //   warp 1      TMEM owner; lane 0 issues, per block j, S_{j+1} then dQ_{j-1}:
 //                 S  = Q K^T      TS  (A = Q bf16 in TMEM, B = K_j K-major)   -> TMEM S
 //                 dQ += dS K      TS  (A = dS bf16 in TMEM, B = K_j MN-major) -> TMEM dQ

@@ -23,7 +23,8 @@
 //               thread), exchanging the row max through shared memory.  P is written
 //               back into the S buffer it came from as two bf16 tiles (Pq in columns
 //               0-63, P in 64-127), consumed by the TS MMAs.  Epilogue: warps 3-6 store
-//               O_q and lse, warps 7-10 O_hp.
+//               O_q and lse, warps 7-10 O_hp; at the end of the item, or (short items,
+//               the kDefer instance) after the next item's first block of P.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O_q [256,256+D), O_hp [256+D,256+2D).
 //
 // The running max is updated only when it grows by more than 8 (base-2 units), so P
