@@ -82,8 +82,10 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int Nkv, int D, i
 // stores fp32 partial sums of dV and dK (the CTA's first segment in slot 2c, its last in
 // 2c + 1), and one more kernel adds an item's segments in CTA order, so the result stays
 // deterministic.  Each range has at least 4 units.  The choice compares estimated
-// makespans, ~2 blocks of fixed cost per item or segment, for 152 SMs, from the sizes
-// alone, so the workspace size is a function of the sizes too.  With many items the
+// makespans for 152 SMs, from the sizes alone, so the workspace size is a function of
+// the sizes too: ~2 blocks of fixed cost per item without the split, ~5 per segment with
+// it (measured: B1 H24 N4608 ran 9% and B2 H8 Nq4096 Nkv1024 17% slower split, where ~2
+// per segment had predicted a gain).  With many items the
 // ragged wave costs little and the head-major item order, which keeps the CTAs running
 // together on one head's Q and dO in L2, is kept: returns 0.
 inline int bwd_stream_k_ctas(int B, int H, int Nq, int Nkv) {
@@ -98,7 +100,7 @@ inline int bwd_stream_k_ctas(int B, int H, int Nq, int Nkv) {
   if (G < 1) return 0;
   const double classic = static_cast<double>((items + kSms - 1) / kSms) * (M + 2);
   const double per_cta = static_cast<double>(W) / G;
-  const double split = per_cta + 2.0 * (per_cta / M + 2.0);
+  const double split = per_cta + 5.0 * (per_cta / M + 2.0);
   return split < 0.95 * classic ? static_cast<int>(G) : 0;
 }
 

@@ -56,7 +56,7 @@ def test_page_backward_c1():
 
 @pytest.mark.parametrize("B,H,N,D,causal", [(1, 2, 200, 128, True), (2, 1, 130, 64, False),
                                             (1, 1, 65, 128, True),
-                                            (1, 1, 1000, 64, False)])  # dK/dV stream-K, items in 2 segments
+                                            (1, 1, 2048, 64, False)])  # dK/dV stream-K: 64 ranges of 4 blocks
 def test_page_backward_edges(B, H, N, D, causal):
     inp = custom_inputs(1200 + N, B, H, N, N, D)
     _check(inp, causal, 1.0 / np.sqrt(D), [(b, h) for b in range(B) for h in range(H)])

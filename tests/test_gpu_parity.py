@@ -119,7 +119,7 @@ def test_c5b_cross_attention_sampled_heads():
     (2, 1, 100, 37, 64, False),
     (1, 1, 200, 200, 128, True),
     (1, 1, 7, 300, 128, False),
-    (1, 2, 1100, 300, 128, False),  # few (head, key block) items: stream-K ranges
+    (1, 2, 1100, 300, 128, False),  # few (head, key block) items, one CTA each
     (1, 1, 2000, 130, 64, False),   # stream-K, items in 4 segments, D = 64
 ])
 def test_edge_shapes(B, H, Nq, Nkv, D, causal):
