@@ -157,7 +157,7 @@ def test_deterministic(causal):
         assert torch.equal(a[n], b[n]), n
 
 
-def test_deterministic_with_query_parts():
+def test_deterministic_stream_k():
     """With few (head, key block) items the dK/dV kernel runs stream-K: equal ranges of
     the items' query blocks per CTA, cut items storing fp32 partial sums that a second
     kernel adds in CTA order, so dK and dV stay bit-identical run to run."""
@@ -193,7 +193,7 @@ def test_inputs_16_byte_aligned_match_aligned():
         assert torch.equal(a[n], t), n
 
 
-def test_query_part_split_without_room_for_its_sums_runs_unsplit():
+def test_stream_k_without_room_for_its_sums_runs_one_cta_per_item():
     """A workspace that holds everything but the dK/dV segments' partial sums (as the
     no-alloc scratch may) runs the backward with one CTA per item instead of stream-K:
     the same gradients up to the fp32 summation order.  One byte less than that is
