@@ -697,6 +697,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
     const int q = valid ? static_cast<int>(rw % nq_pad) : 0;
     const bool in = valid && q < a.Nq;
     float acc = 0.f;
+    // the row's lse is loaded with its O_hp and dO, not after the sum: one memory
+    // latency per pass instead of two
+    const float lse = in ? a.lse[bh * a.Nq + q] : 0.f;
     if (in) {
       const long long src = (bh * a.Nq + q) * D + 8 * sub;
       const uint4 ov = *reinterpret_cast<const uint4*>(a.o_hp + src);
@@ -715,7 +718,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
     for (int off = kLanesPerRow / 2; off > 0; off >>= 1)   // within the row's lanes
       acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (!valid) continue;
-    const float lse = in ? a.lse[bh * a.Nq + q] : 0.f;
     if (sub == 0) {
       a.delta[rw] = in ? acc : 0.f;
       a.lse_pad[rw] = in ? lse : INFINITY;
