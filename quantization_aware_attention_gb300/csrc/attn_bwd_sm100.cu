@@ -65,6 +65,7 @@ using namespace sm100;
 constexpr int kBlk = 128;       // keys per item, queries per block
 constexpr int kThreads = 352;
 constexpr int kPrefetch = 3;    // query blocks between an L2 prefetch and the block's load
+constexpr int kMaxSkCtas = 160; // stream-K CTAs at most (bwd_stream_k_ctas caps them at 152)
 
 template <int D>
 struct BwdTc {
@@ -737,45 +738,45 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int nq_pad) {
   }
 }
 
-// Stream-K fix-up: for every item that range boundaries cut, adds its segments' fp32
-// partial sums in CTA order (the CTAs c0..c1 whose ranges meet the item; a segment sits
-// in slot 2c when it is CTA c's first, else 2c + 1) and stores bf16 dV and dK (x
-// sm_scale).  One thread per 4 columns of one key row of dV or dK.  Items inside one
-// range were stored by the dK/dV kernel directly.
+// Stream-K fix-up, blockIdx.x = item: for an item that range boundaries cut, adds its
+// segments' fp32 partial sums in CTA order (the CTAs c0..c1 whose ranges meet the item;
+// a segment sits in slot 2c when it is CTA c's first, else 2c + 1) and stores bf16 dV
+// and dK (x sm_scale).  Items inside one range were stored by the dK/dV kernel directly.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_segment_sum_kernel(const float4* __restrict__ part,
                                                               int work, int G, int mtiles,
-                                                              int ktiles, long long items,
-                                                              int Nkv, float sm_scale,
+                                                              int ktiles, int Nkv, float sm_scale,
                                                               uint2* dv, uint2* dk) {
   constexpr int kD4 = D / 4;
-  const long long per_item = 2ll * kBlk * kD4;
-  const long long stride = static_cast<long long>(gridDim.x) * 256;
-  for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < items * per_item;
-       i += stride) {
-    const long long item = i / per_item;
-    const int rem = static_cast<int>(i - item * per_item);
-    const int t = rem / (kBlk * kD4);                    // 0: dV, 1: dK
-    const int row = (rem / kD4) % kBlk;
-    const int c4 = rem % kD4;
-    const int kb = static_cast<int>(item % ktiles);
-    if (kb * kBlk + row >= Nkv) continue;
-    const long long first = item * mtiles, last = first + mtiles - 1;
-    // CTA whose range holds unit u: the last c with work c / G <= u
-    const int c0 = static_cast<int>(((first + 1) * G - 1) / work);
-    const int c1 = static_cast<int>(((last + 1) * G - 1) / work);  // (64-bit products)
-    if (c0 == c1) continue;
+  __shared__ int slot_of[kMaxSkCtas];
+  const int item = blockIdx.x;
+  const long long first = static_cast<long long>(item) * mtiles, last = first + mtiles - 1;
+  // CTA whose range holds unit u: the last c with work c / G <= u (64-bit products)
+  const int c0 = static_cast<int>(((first + 1) * G - 1) / work);
+  const int c1 = static_cast<int>(((last + 1) * G - 1) / work);
+  if (c0 == c1) return;
+  for (int c = c0 + static_cast<int>(threadIdx.x); c <= c1; c += blockDim.x)
+    slot_of[c - c0] = 2 * c + (sk_start(work, c, G) >= first ? 0 : 1);
+  __syncthreads();
+  const int kb = item % ktiles;
+  const long long bh = item / ktiles;
+  const int rows = min(kBlk, Nkv - kb * kBlk);
+  // blockIdx.y takes every gridDim.y-th group of 256 of the item's 2 x 128 x D/4 float4s
+  for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < 2 * kBlk * kD4;
+       i += gridDim.y * blockDim.x) {
+    const int t = i / (kBlk * kD4);                    // 0: dV, 1: dK
+    const int row = (i / kD4) % kBlk;
+    const int c4 = i % kD4;
+    if (row >= rows) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c0; c <= c1; ++c) {
-      const long long slot = 2ll * c + (sk_start(work, c, G) >= first ? 0 : 1);
-      const float4 x = part[((slot * 2 + t) * kBlk + row) * kD4 + c4];
+    for (int c = 0; c <= c1 - c0; ++c) {
+      const float4 x = part[((static_cast<long long>(slot_of[c]) * 2 + t) * kBlk + row) * kD4 + c4];
       acc.x += x.x;
       acc.y += x.y;
       acc.z += x.z;
       acc.w += x.w;
     }
     const float sc = t ? sm_scale : 1.0f;
-    const long long bh = item / ktiles;
     const long long o = ((bh * Nkv) + kb * kBlk + row) * kD4 + c4;
     (t ? dk : dv)[o] = make_uint2(pack_bf16x2(acc.x * sc, acc.y * sc), pack_bf16x2(acc.z * sc, acc.w * sc));
   }
@@ -825,12 +826,9 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.streamk) {
-    const long long n = static_cast<long long>(p.items) * 2 * kBlk * (D / 4);
-    long long blocks = (n + 255) / 256;
-    if (blocks > static_cast<long long>(num_sms) * 16) blocks = static_cast<long long>(num_sms) * 16;
-    bwd_segment_sum_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(a.part), p.work, G, p.mtiles, p.ktiles, p.items, a.Nkv,
-        a.sm_scale, reinterpret_cast<uint2*>(a.dv), reinterpret_cast<uint2*>(a.dk));
+    bwd_segment_sum_kernel<D><<<dim3(p.items, 2 * kBlk * (D / 4) / 512), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(a.part), p.work, G, p.mtiles, p.ktiles, a.Nkv, a.sm_scale,
+        reinterpret_cast<uint2*>(a.dv), reinterpret_cast<uint2*>(a.dk));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
