@@ -174,11 +174,20 @@ __device__ __forceinline__ int bwd_step(int idx, const BwdItem& t) {
   else return idx + static_cast<int>(gridDim.x);
 }
 
-// query block of the item's ii-th step
+// query block of the item's ii-th step.  Stream-K segments are walked from their last
+// query block down: a CTA's first segment usually runs to its item's end, so the CTAs
+// that start the key blocks of one head part-way through its query blocks (their ranges
+// begin 134.7 units apart at B1 H40 Nq16384 Nkv512) then read the same blocks together
+// and share them in L2.
+template <bool kSK>
 __device__ __forceinline__ int block_at(const BwdItem& t, int ii) {
-  int b = t.rot + ii;
-  if (b >= t.count) b -= t.count;
-  return t.q0 + b;
+  if constexpr (kSK) {
+    return t.q0 + t.count - 1 - ii;
+  } else {
+    int b = t.rot + ii;
+    if (b >= t.count) b -= t.count;
+    return t.q0 + b;
+  }
 }
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -277,9 +286,9 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(base + C::kOffV + c * C::kChunkBytes, &tmV, bar(B_KV_FULL), 64 * c,
                       kb * kBlk, bh);
         }
-        ok = load_q(bh, block_at(t, 0));
+        ok = load_q(bh, block_at<kSK>(t, 0));
         for (int ii = 0; ii < count && ok; ++ii) {
-          const int blk = block_at(t, ii);
+          const int blk = block_at<kSK>(t, ii);
           const uint32_t dst = dc & 1, duse = dc >> 1;
           ok = mbar_wait(bar(B_DO_EMPTY0 + dst), (duse & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(384, 1)
           // DRAM, which the two-stage rings alone do not cover.  (With one CTA per item
           // the CTAs share one head and the prefetches only add L2 traffic: 5% slower.)
           if (kSK && ii + kPrefetch < count) {
-            const int pb = block_at(t, ii + kPrefetch) * kBlk;
+            const int pb = block_at<kSK>(t, ii + kPrefetch) * kBlk;
             for (int c = 0; c < C::kChunks; ++c) {
               tma_prefetch_l2_3d(&tmQ, 64 * c, pb, bh);
               tma_prefetch_l2_3d(&tmDO, 64 * c, pb, bh);
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(384, 1)
             tma_prefetch_l2_3d(&tmQX, 0, pb, bh);
             tma_prefetch_l2_3d(&tmDX, 0, pb, bh);
           }
-          if (ii + 1 < count) ok = load_q(bh, block_at(t, ii + 1));
+          if (ii + 1 < count) ok = load_q(bh, block_at<kSK>(t, ii + 1));
         }
       }
       // drain: every issued load lands before the CTA exits
@@ -608,10 +617,10 @@ __global__ void __launch_bounds__(384, 1)
         return p.a.page_bwd ? p_phase_page(c_, blk_, kb, key_ok, key)
                             : p_phase(c_, blk_, kb, key_ok, key);
       };
-      ok = pp(qc, block_at(t, 0));
+      ok = pp(qc, block_at<kSK>(t, 0));
       for (int ii = 0; ii < count && ok; ++ii, ++qc) {
         ok = ds_phase(qc);
-        if (ok && ii + 1 < count) ok = pp(qc + 1, block_at(t, ii + 1));
+        if (ok && ii + 1 < count) ok = pp(qc + 1, block_at<kSK>(t, ii + 1));
       }
       if (!ok) break;
       // ---- epilogue: h = 0 stores dV, h = 1 stores dK for this item's key rows
