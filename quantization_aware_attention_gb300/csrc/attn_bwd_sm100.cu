@@ -805,6 +805,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, unsigned int* err, int num_sms, cu
   const long long work = static_cast<long long>(p.items) * p.mtiles;
   int G = a.causal || a.part == nullptr ? 0 : a.sk_ctas;
   if (G > num_sms) G = num_sms;
+  if (G > kMaxSkCtas) G = kMaxSkCtas;  // the fix-up's shared slot table
   if (G > 0 && (work < 4ll * G || work > (1ll << 30))) G = 0;
   p.work = G > 0 ? static_cast<int>(work) : 0;
   p.streamk = G > 0;
